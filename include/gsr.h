@@ -1,0 +1,141 @@
+/*
+ * gsr.h - fused GEMM + scale + ReLU on GB300 (sm_103a):
+ *
+ *     C[m,n] = ReLU( alpha * sum_{k=0}^{K-1} A[m,k] * B[k,n] )
+ *
+ * Operator definition: "Tutorial14: 使用TileLang语言编写attention算子" (PKUHPC
+ * scow-tutorial), section 3 (算子介绍) gives the formula and ReLU(x) = max(x, 0);
+ * section 2 (编写算子), the gemm_fused kernel, fixes the data types (A, B, C
+ * float16, accumulator float32, scale float32) and the order of the epilogue
+ * (multiply by the scale first, then the max with 0, then the fp16 store).
+ *
+ * Plain C ABI: pointers and sizes only.  Every entry point returns a
+ * gsr_status and never aborts the process.  Entry points that launch work are
+ * asynchronous on the given stream: returning GSR_OK means the work was
+ * queued, not that it finished.  A NULL stream is the legacy default stream.
+ * Thread-safety: the entry points may be called from several host threads.
+ */
+#ifndef GSR_H_
+#define GSR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; declared here so this header needs no
+ * CUDA header. */
+struct CUstream_st;
+
+typedef enum gsr_status {
+    GSR_OK = 0,
+    /* A negative size, a size above 2^31 - 1, a NULL pointer where data is
+     * needed, or a NULL stream pointer argument where one is required. */
+    GSR_ERR_INVALID_ARG = 1,
+    /* A, B or C not 16-byte aligned, or N or K not a multiple of 8 (the tensor
+     * copy engine needs every row pitch to be a multiple of 16 bytes). */
+    GSR_ERR_ALIGNMENT = 2,
+    /* C overlaps A or B. */
+    GSR_ERR_ALIAS = 3,
+    /* A CUDA runtime call failed; gsr_last_cuda_error() has its code. */
+    GSR_ERR_CUDA = 4,
+    /* A kernel gave up on a bounded wait (reported by gsr_device_status). */
+    GSR_ERR_DEVICE_TIMEOUT = 5,
+    /* The current device is not compute capability 10.3 (GB300). */
+    GSR_ERR_UNSUPPORTED_DEVICE = 6
+} gsr_status;
+
+/*
+ * C = ReLU(alpha * A.B).
+ *
+ *   A      device pointer, M x K float16, row-major (row stride K elements).
+ *   B      device pointer, K x N float16, row-major (row stride N elements).
+ *   C      device pointer, M x N float16, row-major (row stride N elements);
+ *          written, never read.  Must not overlap A or B.
+ *   M,N,K  sizes, 0 <= M, N, K <= 2^31 - 1; N and K multiples of 8.
+ *   alpha  float32 scale, applied to the float32 sum before the ReLU.
+ *   stream CUDA stream the work is queued on (NULL: legacy default stream).
+ *
+ * All three buffers are owned by the caller and must stay valid until the
+ * work on `stream` has finished.  Results: the sum is carried in float32 on
+ * the tensor cores and rounded once to float16 (nearest, ties to even).
+ * ReLU of -0 or NaN gives 0.  M == 0 or N == 0: nothing to do, GSR_OK.
+ * K == 0: C is filled with zeros (ReLU(alpha * 0)).
+ *
+ * Paths: M <= 64 runs the small-M kernel (B streamed once, K split across
+ * SMs), otherwise the tiled kernel.
+ *
+ * Device memory the library owns: on the first call on each (device, stream)
+ * pair it allocates a 4-byte error word for that stream, and the small-M
+ * kernel keeps fp32 partial tiles and per-tile ticket counters in a workspace
+ * allocated (or grown) on the first small-M call on the pair.  Both stay
+ * until gsr_shutdown().  Calls on different streams never share them; such a
+ * first call synchronises its stream and so should not be made during stream
+ * capture.
+ */
+gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                           int64_t K, float alpha, struct CUstream_st* stream);
+
+/*
+ * gemm_scale_relu with the operands in host memory: copies A and B host ->
+ * device into the caller's device buffers dA and dB, runs gemm_scale_relu
+ * into dC and copies C back device -> host, all queued on `stream`.  The host
+ * buffers should be page-locked (cudaHostAlloc / pinned) for the copies to be
+ * asynchronous.  hC holds the result once the stream has finished.  Sizes,
+ * alignment and errors as for gemm_scale_relu; dC must not overlap dA or dB.
+ */
+gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* dA, void* dB,
+                                void* dC, int64_t M, int64_t N, int64_t K, float alpha,
+                                struct CUstream_st* stream);
+
+/*
+ * Waits for `stream`, then reads and clears the error word of the (current
+ * device, stream) pair.  Returns GSR_ERR_DEVICE_TIMEOUT if a kernel queued on
+ * that stream since the last call gave up on a bounded wait (the pair's
+ * small-M ticket counters are then reset too), GSR_ERR_CUDA if the stream
+ * reported an error, else GSR_OK.  `code` (may be NULL) receives the raw
+ * device error code, 0 if none: low byte = which wait gave up (1 producer
+ * waiting for a free stage, 2 MMA issuer waiting for loaded data, 3 MMA issuer
+ * waiting for a free accumulator, 4 epilogue waiting for a finished
+ * accumulator, 5 teardown drain), 0x100 = tiled kernel, 0x200 = small-M.
+ */
+gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
+
+/* Path the library would take for these sizes: 0 = tiled, 1 = small-M. */
+int gsr_select_path(int64_t M, int64_t N, int64_t K);
+
+/* Forces a path for later calls (process-wide): 0 = automatic (default),
+ * 1 = tiled with automatic tile width, 2 = small-M (only honoured when
+ * M <= 64), 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles.
+ * For tests and measurements. */
+void gsr_set_path_override(int path);
+
+/* Upper bound, in nanoseconds, on every wait inside the kernels (default 1 s).
+ * A wait that runs out records an error (see gsr_device_status) and the kernel
+ * exits early, leaving C incomplete. */
+void gsr_set_wait_timeout_ns(uint64_t ns);
+
+/* Test-only switches, 0 in normal use.  Bit 0: the first CTA's producer skips
+ * its first shared-memory fill, so that CTA's waits run out (exercises the
+ * bounded-wait path without faulting the GPU). */
+void gsr_set_test_flags(uint32_t flags);
+
+/* CUDA error code of the last failing CUDA call on this host thread (0: none). */
+int gsr_last_cuda_error(void);
+
+/* Static, human-readable name of a status. */
+const char* gsr_status_string(gsr_status s);
+
+/* Library version string, e.g. "gsr 0.1.0 sm_103a". */
+const char* gsr_version(void);
+
+/* Frees every workspace and error word the library holds, on every device.
+ * Must not run while work queued by the library is still executing. */
+gsr_status gsr_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSR_H_ */

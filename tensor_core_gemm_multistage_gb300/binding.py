@@ -1,0 +1,217 @@
+"""ctypes binding of libgsr: the same entry points as include/gsr.h, with argument
+marshalling only.  Every step of C = ReLU(alpha * A @ B) runs in the library's CUDA
+kernels; there is no Python or CPU fallback.  If libgsr.so is missing, the first call
+raises instead of computing anything.
+
+PyTorch is used only to hand over device memory and streams: tensors are passed as
+raw pointers plus sizes, streams as their CUDA handles.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+from . import _build
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_INVALID_ARG = 1
+    ERR_ALIGNMENT = 2
+    ERR_ALIAS = 3
+    ERR_CUDA = 4
+    ERR_DEVICE_TIMEOUT = 5
+    ERR_UNSUPPORTED_DEVICE = 6
+
+
+class GsrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        msg = "%s failed: %s" % (what, status_string(status))
+        if status == Status.ERR_CUDA:
+            msg += " (CUDA error %d)" % last_cuda_error()
+        super().__init__(msg)
+
+
+PATH_AUTO, PATH_TILED, PATH_SKINNY, PATH_TILED_256, PATH_TILED_128 = 0, 1, 2, 3, 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgsr.so; raises ImportError when it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(
+                "libgsr.so not found at %s; build it first with "
+                "`python -m tensor_core_gemm_multistage_gb300._build`" % path)
+        L = ctypes.CDLL(path)
+        vp, i64, f32, u32, u64, i32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
+                                       ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int)
+        L.gemm_scale_relu.restype = i32
+        L.gemm_scale_relu.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
+        L.gemm_scale_relu_host.restype = i32
+        L.gemm_scale_relu_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, vp]
+        L.gsr_device_status.restype = i32
+        L.gsr_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        L.gsr_select_path.restype = i32
+        L.gsr_select_path.argtypes = [i64, i64, i64]
+        L.gsr_set_path_override.restype = None
+        L.gsr_set_path_override.argtypes = [i32]
+        L.gsr_set_wait_timeout_ns.restype = None
+        L.gsr_set_wait_timeout_ns.argtypes = [u64]
+        L.gsr_set_test_flags.restype = None
+        L.gsr_set_test_flags.argtypes = [u32]
+        L.gsr_last_cuda_error.restype = i32
+        L.gsr_last_cuda_error.argtypes = []
+        L.gsr_status_string.restype = ctypes.c_char_p
+        L.gsr_status_string.argtypes = [i32]
+        L.gsr_version.restype = ctypes.c_char_p
+        L.gsr_version.argtypes = []
+        L.gsr_shutdown.restype = i32
+        L.gsr_shutdown.argtypes = []
+        _lib = L
+        return L
+
+
+# ---------------------------------------------------------------------------- raw C ABI
+
+def gemm_scale_relu_ptr(A: int, B: int, C: int, M: int, N: int, K: int, alpha: float,
+                        stream: int = 0) -> int:
+    """The C entry point with raw integer pointers; returns the gsr_status code."""
+    return lib().gemm_scale_relu(A or None, B or None, C or None, M, N, K, ctypes.c_float(alpha),
+                                 stream or None)
+
+
+def gemm_scale_relu_host_ptr(hA: int, hB: int, hC: int, dA: int, dB: int, dC: int, M: int, N: int,
+                             K: int, alpha: float, stream: int = 0) -> int:
+    return lib().gemm_scale_relu_host(hA or None, hB or None, hC or None, dA or None, dB or None,
+                                      dC or None, M, N, K, ctypes.c_float(alpha), stream or None)
+
+
+def select_path(M: int, N: int, K: int) -> int:
+    return int(lib().gsr_select_path(M, N, K))
+
+
+def set_path_override(path: int) -> None:
+    lib().gsr_set_path_override(int(path))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib().gsr_set_wait_timeout_ns(int(ns))
+
+
+def set_test_flags(flags: int) -> None:
+    lib().gsr_set_test_flags(int(flags))
+
+
+def last_cuda_error() -> int:
+    return int(lib().gsr_last_cuda_error())
+
+
+def status_string(status: int) -> str:
+    return lib().gsr_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().gsr_version().decode()
+
+
+def shutdown() -> None:
+    s = lib().gsr_shutdown()
+    if s != Status.OK:
+        raise GsrError(s, "gsr_shutdown")
+
+
+# ---------------------------------------------------------------------------- torch tensors
+
+def _stream_handle(stream, device) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_matrix(t, name, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != torch.float16:
+        raise TypeError("%s must be float16, got %s" % (name, t.dtype))
+    if t.dim() != 2:
+        raise ValueError("%s must be 2-D, got shape %s" % (name, tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous (row-major)" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def gemm_scale_relu(A, B, C, alpha: float, stream=None):
+    """C = ReLU(alpha * A @ B) into the preallocated fp16 tensor C (returned).
+
+    A (M, K), B (K, N), C (M, N): contiguous float16 CUDA tensors on one device.
+    Queued on ``stream`` (default: the current torch stream of that device).
+    """
+    import torch
+    _check_matrix(A, "A")
+    M, K = A.shape
+    _check_matrix(B, "B")
+    if B.shape[0] != K:
+        raise ValueError("inner sizes differ: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    N = B.shape[1]
+    _check_matrix(C, "C", (M, N))
+    dev = C.device
+    if dev.type != "cuda" or A.device != dev or B.device != dev:
+        raise ValueError("A, B and C must be CUDA tensors on one device")
+    with torch.cuda.device(dev):
+        s = lib().gemm_scale_relu(A.data_ptr() or None, B.data_ptr() or None, C.data_ptr() or None,
+                                  M, N, K, ctypes.c_float(alpha), _stream_handle(stream, dev) or None)
+    if s != Status.OK:
+        raise GsrError(s, "gemm_scale_relu")
+    return C
+
+
+def gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, alpha: float, stream=None):
+    """Host-memory variant: hA, hB (pinned CPU fp16) are copied into dA, dB, the product
+    is computed into dC and copied back into hC (pinned CPU fp16), all on ``stream``."""
+    import torch
+    _check_matrix(hA, "hA")
+    M, K = hA.shape
+    _check_matrix(hB, "hB")
+    N = hB.shape[1]
+    _check_matrix(hC, "hC", (M, N))
+    _check_matrix(dA, "dA", (M, K))
+    _check_matrix(dB, "dB", (K, N))
+    _check_matrix(dC, "dC", (M, N))
+    dev = dC.device
+    with torch.cuda.device(dev):
+        s = lib().gemm_scale_relu_host(hA.data_ptr() or None, hB.data_ptr() or None,
+                                       hC.data_ptr() or None, dA.data_ptr() or None,
+                                       dB.data_ptr() or None, dC.data_ptr() or None, M, N, K,
+                                       ctypes.c_float(alpha), _stream_handle(stream, dev) or None)
+    if s != Status.OK:
+        raise GsrError(s, "gemm_scale_relu_host")
+    return hC
+
+
+def device_status(stream=None, device=None):
+    """Waits for ``stream`` and returns (Status, raw device error code)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    code = ctypes.c_int(0)
+    with torch.cuda.device(dev):
+        s = lib().gsr_device_status(_stream_handle(stream, dev) or None, ctypes.byref(code))
+    return Status(s), int(code.value)

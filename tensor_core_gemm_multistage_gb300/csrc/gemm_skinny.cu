@@ -1,0 +1,327 @@
+// gemm_skinny.cu - small-M path of C = ReLU(alpha * A.B) on sm_103a (M <= 64).
+//
+// Same operator as the tiled path ("Tutorial14: 使用TileLang语言编写attention算子",
+// section 3 formula; section 2 kernel: float accumulator, scale, max with 0, fp16 out).
+// When M is a handful of rows the work is streaming B (K x N) from HBM once; a 128-row
+// M tile would leave most of each MMA empty and only ceil(N/BN) CTAs busy.  So:
+//  * swap A and B: the MMA computes C^T (N x M) = B^T (N x K) . A^T (K x M), with
+//    128 columns of C per tile as the MMA's M and M (rounded up to MP = 16/32/64) as
+//    its N.  B^T is read straight from row-major B as an MN-major operand and A^T from
+//    row-major A as a K-major operand: nothing is transposed in memory;
+//  * stream-K: the (tile, 64-wide k block) units are laid out tile-major and CTA p of
+//    P owns the contiguous run [p*T/P, (p+1)*T/P), so every SM streams the same number
+//    of B bytes.  A run that covers a whole tile stores it directly; a run that covers
+//    part of a tile writes an fp32 partial into its own slot of the workspace and takes
+//    a ticket; the CTA whose ticket completes the tile's k count sums the partials in
+//    fixed CTA order (deterministic), applies scale + ReLU + fp16 and resets the
+//    ticket to 0 for the next launch.  Nobody waits on another CTA, so nothing can
+//    deadlock across CTAs.
+#include <atomic>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace gsr {
+namespace {
+
+template <int MP_, int STAGES_>
+struct SkinnyCfg {
+    static constexpr int TN = 128;          // columns of C per tile (MMA M)
+    static constexpr int BK = 64;
+    static constexpr int MP = MP_;          // MMA N: M rounded up to a multiple of 16
+    static constexpr int STAGES = STAGES_;
+    static constexpr int NUM_THREADS = 192;
+    static constexpr int BT_CHUNK_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
+    static constexpr int BT_STAGE_BYTES = BK * TN * 2;   // 16 KB
+    static constexpr int AT_STAGE_BYTES = MP * BK * 2;   // MP rows of A, 128 bytes each
+    static constexpr int STAGE_BYTES = BT_STAGE_BYTES + AT_STAGE_BYTES;
+    static constexpr int TMEM_COLS = (2 * MP <= 32) ? 32 : (2 * MP <= 64 ? 64 : 128);
+    static constexpr int OFF_BT = 0;
+    static constexpr int OFF_AT = OFF_BT + STAGES * BT_STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_AT + STAGES * AT_STAGE_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM base, abort flag, ticket result
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr uint32_t IDESC = idesc_f16_f32(TN, MP, /*a_mn=*/true, /*b_mn=*/false);
+
+    static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MP must be 16, 32, 48 or 64");
+    static_assert(AT_STAGE_BYTES % 1024 == 0, "A^T stage must keep 1024-byte alignment");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
+};
+
+// Owner of unit x when CTA p owns [floor(p*T/P), floor((p+1)*T/P)).
+__device__ __forceinline__ int unit_owner(long long x, long long T, int P) {
+    return (int)(((x + 1) * (long long)P + T - 1) / T) - 1;
+}
+__device__ __forceinline__ long long cta_begin(int p, long long T, int P) {
+    return (long long)p * T / P;
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
+    gsr_skinny_kernel(const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmAt,
+                      const SkinnyParams p) {
+    constexpr int S = Cfg::STAGES;
+    constexpr int MP = Cfg::MP;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+
+    auto full_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (S + s); };
+    auto tfull_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + a); };
+    auto tempty_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * S + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 4);
+    volatile int* s_last = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long T = p.total_units;
+    const int P = p.num_ctas;
+    const int kbpt = p.num_k_blocks;
+    const long long my_begin = cta_begin(blockIdx.x, T, P);
+    const long long my_end = cta_begin(blockIdx.x + 1, T, P);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 128);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmBt);
+        tma_prefetch_desc(&tmAt);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish_alloc_permit();
+    }
+    tcgen05_fence_before();
+    __syncthreads();
+    tcgen05_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const Waiter w{p.err, p.timeout_ns, abort_flag, kDevErrKernelSkinny};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        const uint64_t pol_stream = l2_policy_evict_first();   // B: every byte read once
+        const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every CTA
+        uint32_t stage = 0, phase = 0;
+        uint32_t armed_mask = 0, armed_parity = 0;
+        bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+        bool ok = true;
+        for (long long pos = my_begin; ok && pos < my_end;) {
+            const int tile = (int)(pos / kbpt);
+            const int kb0 = (int)(pos % kbpt);
+            const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+            const int n0 = tile * Cfg::TN;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                bool got = true;
+                if (lane == 0) got = w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty);
+                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                if (lane == 0) {
+                    if (drop_first) {
+                        drop_first = false;
+                    } else {
+                        const uint32_t fb = full_bar(stage);
+                        const uint32_t bt = sb + Cfg::OFF_BT + stage * Cfg::BT_STAGE_BYTES;
+                        mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                        tma_load_2d_hint(bt, &tmBt, fb, n0, kb * Cfg::BK, pol_stream);
+                        tma_load_2d_hint(bt + Cfg::BT_CHUNK_BYTES, &tmBt, fb, n0 + 64, kb * Cfg::BK,
+                                         pol_stream);
+                        tma_load_2d_hint(sb + Cfg::OFF_AT + stage * Cfg::AT_STAGE_BYTES, &tmAt, fb,
+                                         kb * Cfg::BK, 0, pol_keep);
+                        armed_mask |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                }
+                __syncwarp();
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+            pos += kb1 - kb0;
+        }
+        if (lane == 0)
+            for (int s = 0; s < S; ++s)
+                if (armed_mask & (1u << s)) w.drain(full_bar(s), (armed_parity >> s) & 1u);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        uint32_t stage = 0, phase = 0, it = 0;
+        bool ok = true;
+        for (long long pos = my_begin; ok && pos < my_end; ++it) {
+            const int kb0 = (int)(pos % kbpt);
+            const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+            const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
+            bool got = true;
+            if (lane == 0) got = w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty);
+            if (!__shfl_sync(0xffffffffu, got, 0)) break;
+            tcgen05_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * MP;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (lane == 0) got = w.wait(full_bar(stage), phase, kDevErrMmaFull);
+                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                tcgen05_fence_after();
+                if (lane == 0) {
+                    const uint32_t bt = sb + Cfg::OFF_BT + stage * Cfg::BT_STAGE_BYTES;
+                    const uint32_t at = sb + Cfg::OFF_AT + stage * Cfg::AT_STAGE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 16; ++k) {
+                        // MMA A = B^T: MN-major, 16 K rows = 2048 bytes per step, 64-col chunks 8 KB apart.
+                        const uint64_t ad = smem_desc_sw128(bt + k * 2048, Cfg::BT_CHUNK_BYTES, 1024);
+                        // MMA B = A^T: K-major, 16 elements = 32 bytes per step.
+                        const uint64_t bd = smem_desc_sw128(at + k * 32, 16, 1024);
+                        mma_f16_ss(d_tmem, ad, bd, Cfg::IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(tfull_bar(acc));
+            __syncwarp();
+            pos += kb1 - kb0;
+        }
+        if (lane == 0) {
+            mma_commit(drain_bar);
+            w.drain(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2-5)
+        const int quad = warp & 3;
+        const int nl = quad * 32 + lane;     // column of C inside the tile == TMEM lane
+        const int et = threadIdx.x - 64;
+        uint32_t it = 0;
+        for (long long pos = my_begin; pos < my_end; ++it) {
+            const int tile = (int)(pos / kbpt);
+            const int kb0 = (int)(pos % kbpt);
+            const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+            const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
+            const bool got = w.wait(tfull_bar(acc), acc_parity, kDevErrEpilogueFull);
+            if (!named_bar_and(1, 128, got)) break;
+            tcgen05_fence_after();
+
+            float v[MP];
+            {
+                const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * MP;
+#pragma unroll
+                for (int c = 0; c < MP / 16; ++c) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(t_row + c * 16, r);
+                    tmem_ld_wait(r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
+                }
+            }
+            tcgen05_fence_before();
+            mbar_arrive(tempty_bar(acc));
+
+            const int n = tile * Cfg::TN + nl;
+            bool store = true;
+            if (!(kb0 == 0 && kb1 == kbpt)) {
+                // Part of a tile: publish the partial, take a ticket.
+                const int slot = (pos == my_begin) ? 0 : 1;
+                float* mine = p.partials + ((size_t)blockIdx.x * 2 + slot) * (MP * Cfg::TN);
+#pragma unroll
+                for (int m = 0; m < MP; ++m) mine[m * Cfg::TN + nl] = v[m];
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (et == 0) {
+                    const int add = kb1 - kb0;
+                    const int old = atomicAdd(p.tickets + tile, add);
+                    *s_last = (old + add == kbpt) ? 1 : 0;
+                }
+                named_bar_sync(1, 128);
+                store = (*s_last != 0);
+                if (store) {
+                    // Last contributor: sum every partial of this tile in CTA order.
+                    __threadfence();
+                    const long long u0 = (long long)tile * kbpt;
+                    const int p_first = unit_owner(u0, T, P);
+                    const int p_last = unit_owner(u0 + kbpt - 1, T, P);
+                    float sum[MP];
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
+                    for (int q = p_first; q <= p_last; ++q) {
+                        if (q == (int)blockIdx.x) {
+#pragma unroll
+                            for (int m = 0; m < MP; ++m) sum[m] += v[m];
+                        } else {
+                            const int qslot = (cta_begin(q, T, P) >= u0) ? 0 : 1;
+                            const float* src = p.partials + ((size_t)q * 2 + qslot) * (MP * Cfg::TN);
+#pragma unroll
+                            for (int m = 0; m < MP; ++m) sum[m] += __ldcg(src + m * Cfg::TN + nl);
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) v[m] = sum[m];
+                    if (et == 0) p.tickets[tile] = 0;   // ready for the next launch
+                }
+            }
+            if (store && n < p.N) {
+#pragma unroll
+                for (int m = 0; m < MP; ++m)
+                    if (m < p.M)
+                        p.C[(size_t)m * p.N + n] = __float2half_rn(fmaxf(v[m] * p.alpha, 0.0f));
+            }
+            pos += kb1 - kb0;
+        }
+    }
+
+    tcgen05_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tcgen05_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+using Sk16 = SkinnyCfg<16, 11>;
+using Sk32 = SkinnyCfg<32, 10>;
+using Sk64 = SkinnyCfg<64, 8>;
+
+template <class Cfg>
+cudaError_t launch_cfg(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
+                       cudaStream_t stream) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(gsr_skinny_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    gsr_skinny_kernel<Cfg><<<p.num_ctas, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmBt, tmAt, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int skinny_smem_bytes(int mp) {
+    return mp <= 16 ? Sk16::SMEM_BYTES : (mp <= 32 ? Sk32::SMEM_BYTES : Sk64::SMEM_BYTES);
+}
+
+cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
+                          int mp, cudaStream_t stream) {
+    if (mp == 16) return launch_cfg<Sk16>(tmBt, tmAt, p, stream);
+    if (mp == 32) return launch_cfg<Sk32>(tmBt, tmAt, p, stream);
+    if (mp == 64) return launch_cfg<Sk64>(tmBt, tmAt, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gsr

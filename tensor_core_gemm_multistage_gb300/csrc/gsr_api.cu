@@ -1,0 +1,383 @@
+// gsr_api.cu - the C ABI of libgsr: argument checks, path choice, tensor-map encoding,
+// per-(device, stream) state, and the launches.  See include/gsr.h for the contract.
+//
+// Nothing here computes any part of the operator; every step of C = ReLU(alpha * A.B)
+// runs in the kernels of gemm_tiled.cu and gemm_skinny.cu.  The one exception is
+// K == 0, where the empty sum makes every output ReLU(alpha * 0) = 0 and C is cleared
+// with cudaMemsetAsync.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gsr.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<int> g_path_override{0};
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<uint32_t> g_test_flags{0};
+
+constexpr int kSkinnyMaxM = 64;
+constexpr int kGroupM = 16;
+
+struct StreamState {
+    int* err = nullptr;          // device error word for kernels on this stream
+    float* partials = nullptr;   // small-M split-K partial tiles
+    size_t partial_floats = 0;
+    int* tickets = nullptr;      // small-M per-tile ticket counters (zero between launches)
+    size_t ticket_count = 0;
+};
+
+struct DeviceInfo {
+    int cc_major = 0, cc_minor = 0, num_sms = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, CUstream_st*>, StreamState> g_streams;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+gsr_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return GSR_ERR_CUDA;
+}
+
+gsr_status load_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else if (g_encode_err == cudaSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+    });
+    if (!g_encode) return cuda_fail(g_encode_err);
+    return GSR_OK;
+}
+
+// Row-major fp16 matrix of `rows` x `cols` (cols contiguous) seen as a 2-D tensor map with
+// a box of box_cols x box_rows, 128-byte swizzle, zero fill outside the matrix.
+gsr_status encode_fp16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint32_t box_cols, uint32_t box_rows) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return GSR_ERR_CUDA;
+    }
+    return GSR_OK;
+}
+
+// Checks that need no GPU: sizes, null pointers, alignment, aliasing.  `*nothing` is set
+// when there is no output to produce.
+gsr_status validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                    bool* nothing) {
+    *nothing = false;
+    if (M < 0 || N < 0 || K < 0) return GSR_ERR_INVALID_ARG;
+    if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return GSR_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) {
+        *nothing = true;
+        return GSR_OK;
+    }
+    if (!C) return GSR_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B)) return GSR_ERR_INVALID_ARG;
+    // tile counts must fit the kernels' int arithmetic
+    const uint64_t m_blocks = ((uint64_t)M + 127) / 128, n_blocks = ((uint64_t)N + 127) / 128;
+    if (m_blocks * n_blocks > (uint64_t)INT_MAX) return GSR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) || (N & 7)) return GSR_ERR_ALIGNMENT;
+    if (K > 0) {
+        if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
+            (K & 7))
+            return GSR_ERR_ALIGNMENT;
+        const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), c1 = c0 + (uint64_t)M * N * 2;
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(A), a1 = a0 + (uint64_t)M * K * 2;
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(B), b1 = b0 + (uint64_t)K * N * 2;
+        if ((c0 < a1 && a0 < c1) || (c0 < b1 && b0 < c1)) return GSR_ERR_ALIAS;
+    }
+    return GSR_OK;
+}
+
+gsr_status device_info(int* dev_out, DeviceInfo* info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_devices.find(dev);
+    if (it == g_devices.end()) {
+        DeviceInfo d;
+        if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
+                cudaSuccess)
+            return cuda_fail(e);
+        it = g_devices.emplace(dev, d).first;
+    }
+    *dev_out = dev;
+    *info = it->second;
+    if (info->cc_major != 10 || info->cc_minor != 3) return GSR_ERR_UNSUPPORTED_DEVICE;
+    return GSR_OK;
+}
+
+// Per-(device, stream) state: the error word always, the small-M workspace on demand.
+// Returns a copy of the state (pointers stay valid until gsr_shutdown or regrowth).
+gsr_status stream_state(int dev, cudaStream_t stream, size_t need_partials, size_t need_tickets,
+                        StreamState* out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    StreamState& s = g_streams[{dev, stream}];
+    cudaError_t e;
+    if (!s.err) {
+        if ((e = cudaMalloc(&s.err, sizeof(int))) != cudaSuccess) {
+            s.err = nullptr;
+            return cuda_fail(e);
+        }
+        if ((e = cudaMemsetAsync(s.err, 0, sizeof(int), stream)) != cudaSuccess) return cuda_fail(e);
+    }
+    if (need_partials > s.partial_floats || need_tickets > s.ticket_count) {
+        // Earlier launches on this stream may still use the old buffers.
+        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e);
+        if (need_partials > s.partial_floats) {
+            cudaFree(s.partials);
+            s.partials = nullptr;
+            s.partial_floats = 0;
+            if ((e = cudaMalloc(&s.partials, need_partials * sizeof(float))) != cudaSuccess) {
+                s.partials = nullptr;
+                return cuda_fail(e);
+            }
+            s.partial_floats = need_partials;
+        }
+        if (need_tickets > s.ticket_count) {
+            cudaFree(s.tickets);
+            s.tickets = nullptr;
+            s.ticket_count = 0;
+            if ((e = cudaMalloc(&s.tickets, need_tickets * sizeof(int))) != cudaSuccess) {
+                s.tickets = nullptr;
+                return cuda_fail(e);
+            }
+            s.ticket_count = need_tickets;
+            if ((e = cudaMemsetAsync(s.tickets, 0, need_tickets * sizeof(int), stream)) !=
+                cudaSuccess)
+                return cuda_fail(e);
+        }
+    }
+    *out = s;
+    return GSR_OK;
+}
+
+int choose_path(int64_t M) {
+    const int o = g_path_override.load(std::memory_order_relaxed);
+    if (o == 1 || o == 3 || o == 4) return 0;
+    if (o == 2 && M <= kSkinnyMaxM) return 1;
+    return M <= kSkinnyMaxM ? 1 : 0;
+}
+
+gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
+                     cudaStream_t stream, int dev, const DeviceInfo& info) {
+    StreamState st;
+    gsr_status s = stream_state(dev, stream, 0, 0, &st);
+    if (s != GSR_OK) return s;
+
+    const int mb = (M + 127) / 128;
+    int bn = 256;
+    const int o = g_path_override.load(std::memory_order_relaxed);
+    if (o == 4 || (o != 3 && (long long)mb * ((N + 255) / 256) < info.num_sms)) bn = 128;
+    const int nb = (N + bn - 1) / bn;
+    const int kb = (K + 63) / 64;
+
+    CUtensorMap tmA, tmB, tmC;
+    if ((s = encode_fp16_2d(&tmA, A, M, K, 64, 128)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmC, C, M, N, 64, 128)) != GSR_OK) return s;
+
+    gsr::TiledParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.num_m_blocks = mb;
+    p.num_n_blocks = nb;
+    p.num_k_blocks = kb;
+    p.num_tiles = mb * nb;
+    p.group_m = kGroupM;
+    p.err = st.err;
+    p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    p.test_flags = g_test_flags.load(std::memory_order_relaxed);
+    const int grid = p.num_tiles < info.num_sms ? p.num_tiles : info.num_sms;
+    cudaError_t e = gsr::launch_tiled(tmA, tmB, tmC, p, bn, grid, stream);
+    return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+}
+
+gsr_status run_skinny(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
+                      cudaStream_t stream, int dev, const DeviceInfo& info) {
+    const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    const int n_tiles = (N + 127) / 128;
+    const int kbpt = (K + 63) / 64;
+    const long long T = (long long)n_tiles * kbpt;
+    const int P = (int)(T < info.num_sms ? T : info.num_sms);
+
+    StreamState st;
+    gsr_status s = stream_state(dev, stream, (size_t)P * 2 * mp * 128, (size_t)n_tiles, &st);
+    if (s != GSR_OK) return s;
+
+    CUtensorMap tmBt, tmAt;
+    if ((s = encode_fp16_2d(&tmBt, B, K, N, 64, 64)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmAt, A, M, K, 64, mp)) != GSR_OK) return s;
+
+    gsr::SkinnyParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.num_n_tiles = n_tiles;
+    p.num_k_blocks = kbpt;
+    p.total_units = T;
+    p.num_ctas = P;
+    p.partials = st.partials;
+    p.tickets = st.tickets;
+    p.C = static_cast<__half*>(C);
+    p.err = st.err;
+    p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    p.test_flags = g_test_flags.load(std::memory_order_relaxed);
+    cudaError_t e = gsr::launch_skinny(tmBt, tmAt, p, mp, stream);
+    return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                           float alpha, CUstream_st* stream) {
+    bool nothing = false;
+    gsr_status s = validate(A, B, C, M, N, K, &nothing);
+    if (s != GSR_OK || nothing) return s;
+    int dev = 0;
+    DeviceInfo info;
+    if ((s = device_info(&dev, &info)) != GSR_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
+        return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+    }
+    if ((s = load_encoder()) != GSR_OK) return s;
+    if (choose_path(M) == 1)
+        return run_skinny(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
+    return run_tiled(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
+}
+
+gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* dA, void* dB,
+                                void* dC, int64_t M, int64_t N, int64_t K, float alpha,
+                                CUstream_st* stream) {
+    bool nothing = false;
+    gsr_status s = validate(dA, dB, dC, M, N, K, &nothing);
+    if (s != GSR_OK || nothing) return s;
+    if (!hC || (K > 0 && (!hA || !hB))) return GSR_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K > 0) {
+        if ((e = cudaMemcpyAsync(dA, hA, (size_t)M * K * 2, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(dB, hB, (size_t)K * N * 2, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    if ((s = gemm_scale_relu(dA, dB, dC, M, N, K, alpha, stream)) != GSR_OK) return s;
+    if ((e = cudaMemcpyAsync(hC, dC, (size_t)M * N * 2, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e);
+    return GSR_OK;
+}
+
+gsr_status gsr_device_status(CUstream_st* stream, int* code) {
+    if (code) *code = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    StreamState s;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_streams.find({dev, stream});
+        if (it == g_streams.end() || !it->second.err) return GSR_OK;
+        s = it->second;
+    }
+    int h = 0;
+    if ((e = cudaMemcpy(&h, s.err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e);
+    if (code) *code = h;
+    if (h == 0) return GSR_OK;
+    // A launch that gave up may have left tickets half counted: start clean.
+    if ((e = cudaMemset(s.err, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    if (s.tickets && (e = cudaMemset(s.tickets, 0, s.ticket_count * sizeof(int))) != cudaSuccess)
+        return cuda_fail(e);
+    return GSR_ERR_DEVICE_TIMEOUT;
+}
+
+int gsr_select_path(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    (void)K;
+    return choose_path(M);
+}
+
+void gsr_set_path_override(int path) { g_path_override.store(path, std::memory_order_relaxed); }
+
+void gsr_set_wait_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed);
+}
+
+void gsr_set_test_flags(uint32_t flags) { g_test_flags.store(flags, std::memory_order_relaxed); }
+
+int gsr_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* gsr_status_string(gsr_status s) {
+    switch (s) {
+        case GSR_OK: return "GSR_OK";
+        case GSR_ERR_INVALID_ARG: return "GSR_ERR_INVALID_ARG";
+        case GSR_ERR_ALIGNMENT: return "GSR_ERR_ALIGNMENT";
+        case GSR_ERR_ALIAS: return "GSR_ERR_ALIAS";
+        case GSR_ERR_CUDA: return "GSR_ERR_CUDA";
+        case GSR_ERR_DEVICE_TIMEOUT: return "GSR_ERR_DEVICE_TIMEOUT";
+        case GSR_ERR_UNSUPPORTED_DEVICE: return "GSR_ERR_UNSUPPORTED_DEVICE";
+    }
+    return "GSR_ERR_UNKNOWN";
+}
+
+const char* gsr_version(void) { return "gsr 0.1.0 sm_103a"; }
+
+gsr_status gsr_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = -1;
+    cudaGetDevice(&cur);
+    gsr_status result = GSR_OK;
+    for (auto& kv : g_streams) {
+        if (cudaSetDevice(kv.first.first) != cudaSuccess) continue;
+        StreamState& s = kv.second;
+        cudaError_t e1 = cudaFree(s.err), e2 = cudaFree(s.partials), e3 = cudaFree(s.tickets);
+        if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+            result = cuda_fail(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+        }
+    }
+    g_streams.clear();
+    if (cur >= 0) cudaSetDevice(cur);
+    return result;
+}
+
+}  // extern "C"

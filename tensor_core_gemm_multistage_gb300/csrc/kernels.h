@@ -1,0 +1,68 @@
+// kernels.h - internal interface between the C-ABI layer (gsr_api.cu) and the kernel
+// translation units (gemm_tiled.cu, gemm_skinny.cu).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+namespace gsr {
+
+// Device-side error codes written (first one wins) into the per-device error word.
+// The low byte says which wait gave up, the next byte which kernel.
+enum DeviceError : int {
+    kDevErrNone = 0,
+    kDevErrProducerEmpty = 1,   // producer: no free shared-memory stage
+    kDevErrMmaFull = 2,         // MMA issuer: stage never filled by TMA
+    kDevErrMmaAccEmpty = 3,     // MMA issuer: accumulator never released by the epilogue
+    kDevErrEpilogueFull = 4,    // epilogue: accumulator never committed by the MMA issuer
+    kDevErrTeardown = 5,        // teardown: in-flight copies or MMAs did not drain
+    kDevErrKernelTiled = 0x100,
+    kDevErrKernelSkinny = 0x200,
+};
+
+// Test-only flags (gsr_set_test_flags).
+enum TestFlags : uint32_t {
+    kTestDropFirstLoad = 1u,    // CTA 0's producer skips its first stage fill
+};
+
+struct TiledParams {
+    int M, N, K;
+    float alpha;
+    int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
+    int* err;               // device error word
+    uint64_t timeout_ns;    // bound on every mbarrier wait
+    uint32_t test_flags;
+};
+
+struct SkinnyParams {
+    int M, N, K;
+    float alpha;
+    int num_n_tiles;        // ceil(N / 128)
+    int num_k_blocks;       // ceil(K / 64) per tile
+    long long total_units;  // num_n_tiles * num_k_blocks
+    int num_ctas;           // P: CTA p owns units [p*T/P, (p+1)*T/P)
+    float* partials;        // [num_ctas][2][MP][128] fp32 split-K partial tiles
+    int* tickets;           // [num_n_tiles], zero between launches
+    __half* C;              // (M, N) row-major output
+    int* err;
+    uint64_t timeout_ns;
+    uint32_t test_flags;
+};
+
+// Tiled path: persistent, one 128 x BN output tile per CTA iteration.
+// bn is 128 or 256.  grid = min(num_tiles, num_sms).
+cudaError_t launch_tiled(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                         const TiledParams& p, int bn, int grid, cudaStream_t stream);
+
+// Skinny path (M <= 64): C^T = B^T A^T on 128-row tiles of N, stream-K split of K.
+// mp is the MMA N (16, 32 or 64).
+cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
+                          int mp, cudaStream_t stream);
+
+// Shared-memory bytes a launch needs (for the one-time attribute set-up).
+int tiled_smem_bytes(int bn);
+int skinny_smem_bytes(int mp);
+
+}  // namespace gsr

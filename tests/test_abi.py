@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function that
+include/gsr.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_core_gemm_multistage_gb300 as gsr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gsr.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gsr.build()
+    yield
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)      # drop comments
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for must in ("gemm_scale_relu", "gemm_scale_relu_host", "gsr_device_status", "gsr_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(gsr.library_path())
+    missing = [n for n in _declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_enum_matches_header():
+    text = open(HEADER).read()
+    for name, value in re.findall(r"GSR_(OK|ERR_\w+)\s*=\s*(\d+)", text):
+        assert gsr.Status[name] == int(value)
+        assert gsr.status_string(int(value)) == "GSR_" + name
+
+
+def test_version():
+    assert gsr.version().startswith("gsr ") and "sm_103a" in gsr.version()
+
+
+# Fake, never-dereferenced device addresses: validation must answer before any CUDA call.
+A, B, C = 0x10000, 0x200000, 0x4000000
+
+
+@pytest.mark.parametrize("M,N,K", [(-1, 8, 8), (8, -8, 8), (8, 8, -8), (2 ** 31, 8, 8),
+                                   (8, 2 ** 31, 8), (8, 8, 2 ** 31)])
+def test_bad_sizes(M, N, K):
+    assert gsr.gemm_scale_relu_ptr(A, B, C, M, N, K, 1.0) == gsr.Status.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M,N", [(0, 8), (8, 0), (0, 0)])
+def test_empty_output_is_a_no_op(M, N):
+    assert gsr.gemm_scale_relu_ptr(0, 0, 0, M, N, 8, 1.0) == gsr.Status.OK
+
+
+def test_null_pointers():
+    assert gsr.gemm_scale_relu_ptr(A, B, 0, 4, 8, 8, 1.0) == gsr.Status.ERR_INVALID_ARG
+    assert gsr.gemm_scale_relu_ptr(0, B, C, 4, 8, 8, 1.0) == gsr.Status.ERR_INVALID_ARG
+    assert gsr.gemm_scale_relu_ptr(A, 0, C, 4, 8, 8, 1.0) == gsr.Status.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("a,b,c,N,K", [
+    (A + 8, B, C, 8, 8), (A, B + 2, C, 8, 8), (A, B, C + 4, 8, 8),   # pointers not 16-byte aligned
+    (A, B, C, 12, 8), (A, B, C, 8, 12), (A, B, C, 1, 8), (A, B, C, 8, 1)])   # pitches not 16 bytes
+def test_alignment(a, b, c, N, K):
+    assert gsr.gemm_scale_relu_ptr(a, b, c, 4, N, K, 1.0) == gsr.Status.ERR_ALIGNMENT
+
+
+def test_alias():
+    M, N, K = 64, 64, 64
+    assert gsr.gemm_scale_relu_ptr(A, B, A, M, N, K, 1.0) == gsr.Status.ERR_ALIAS
+    assert gsr.gemm_scale_relu_ptr(A, B, B + 16 * 64, M, N, K, 1.0) == gsr.Status.ERR_ALIAS
+    # C ending exactly where A begins does not overlap
+    assert gsr.gemm_scale_relu_ptr(A, B, A - M * N * 2, M, N, K, 1.0) != gsr.Status.ERR_ALIAS
+
+
+def test_host_entry_validates_the_same_way():
+    assert gsr.gemm_scale_relu_host_ptr(1, 1, 1, A, B, C, -1, 8, 8, 1.0) == gsr.Status.ERR_INVALID_ARG
+    assert gsr.gemm_scale_relu_host_ptr(0, 1, 1, A, B, C, 4, 8, 8, 1.0) == gsr.Status.ERR_INVALID_ARG
+    assert gsr.gemm_scale_relu_host_ptr(1, 1, 1, A, B, A, 4, 8, 8, 1.0) == gsr.Status.ERR_ALIAS
+
+
+def test_path_selection_and_override():
+    try:
+        assert gsr.select_path(16, 16384, 16384) == 1
+        assert gsr.select_path(64, 8, 8) == 1
+        assert gsr.select_path(65, 8, 8) == 0
+        assert gsr.select_path(8192, 8192, 8192) == 0
+        gsr.set_path_override(gsr.PATH_TILED)
+        assert gsr.select_path(16, 16384, 16384) == 0
+        gsr.set_path_override(gsr.PATH_SKINNY)
+        assert gsr.select_path(16, 8, 8) == 1
+        assert gsr.select_path(100, 8, 8) == 0      # small-M path needs M <= 64
+    finally:
+        gsr.set_path_override(gsr.PATH_AUTO)
+
+
+def test_without_a_gpu_a_valid_call_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    s = gsr.gemm_scale_relu_ptr(A, B, C, 4, 8, 8, 1.0)
+    assert s == gsr.Status.ERR_CUDA
+    assert gsr.last_cuda_error() != 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from tensor_core_gemm_multistage_gb300 import _build, binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "libgsr.so"))
+    with pytest.raises(ImportError):
+        binding.lib()

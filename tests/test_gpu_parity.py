@@ -1,0 +1,250 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Acceptance, per element of C:   |gpu - oracle| <= 1e-2 + 1e-2 * |oracle|
+(the tutorial's own check, torch.testing.assert_close(rtol=1e-2, atol=1e-2), in
+"Tutorial14: 使用TileLang语言编写attention算子", section 2), plus
+    relative Frobenius error ||gpu - oracle||_F / ||oracle||_F <= 1e-3
+(the relative-Frobenius `check` the aikraft.ru TileLang tutorial survey recommends for
+fp16), plus exact zeros wherever the oracle's pre-ReLU value alpha * sum is below -1e-2.
+Every output buffer is pre-filled with NaN so an element the kernel never writes fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tensor_core_gemm_multistage_gb300 as gsr
+from tensor_core_gemm_multistage_gb300.workloads import WORKLOADS, make_inputs, sample_rows, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+FROB = 1e-3
+ZERO_BELOW = -1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gsr.build()
+    oracle.build()
+    yield
+    gsr.set_path_override(gsr.PATH_AUTO)
+
+
+def run_gpu(A, B, alpha, path=gsr.PATH_AUTO, stream=None):
+    """A, B: CPU fp16 tensors. Returns C as a CPU fp16 tensor."""
+    dev = torch.device("cuda", 0)
+    dA = A.to(dev)
+    dB = B.to(dev)
+    dC = torch.full((A.shape[0], B.shape[1]), float("nan"), dtype=torch.float16, device=dev)
+    gsr.set_path_override(path)
+    try:
+        gsr.gemm_scale_relu(dA, dB, dC, alpha, stream=stream)
+        status, code = gsr.device_status(stream)
+    finally:
+        gsr.set_path_override(gsr.PATH_AUTO)
+    assert status == gsr.Status.OK, (status, hex(code))
+    return dC.cpu()
+
+
+def check(C_gpu, C_ref, Z_ref, label=""):
+    x = C_gpu.numpy().astype(np.float64) if hasattr(C_gpu, "numpy") else C_gpu.astype(np.float64)
+    y = C_ref.astype(np.float64)
+    assert x.shape == y.shape
+    assert not np.isnan(x).any(), "%s: %d elements never written" % (label, int(np.isnan(x).sum()))
+    err = np.abs(x - y)
+    bound = ATOL + RTOL * np.abs(y)
+    bad = err > bound
+    assert not bad.any(), "%s: %d elements out of tolerance, worst %g at %s" % (
+        label, int(bad.sum()), float(err.max()), np.unravel_index(np.argmax(err - bound), err.shape))
+    ny = np.linalg.norm(y)
+    if ny > 0:
+        rel = np.linalg.norm(x - y) / ny
+        assert rel <= FROB, "%s: relative Frobenius error %g" % (label, rel)
+    neg = Z_ref < ZERO_BELOW
+    assert np.all(x[neg] == 0), "%s: non-zero output where alpha*sum < -1e-2" % label
+
+
+def parity(M, N, K, alpha, path=gsr.PATH_AUTO, seed=0, b_scaled=False, rows=None):
+    A, B = make_inputs(M, N, K, seed=seed, b_std_inv_sqrt_k=b_scaled)
+    C = run_gpu(A, B, alpha, path)
+    if rows is None:
+        ref, z = oracle.gemm_scale_relu(A, B, alpha, return_pre=True)
+        check(C, ref, z, "%dx%dx%d" % (M, N, K))
+    else:
+        ref, z = oracle.gemm_scale_relu(A, B, alpha, rows=rows, return_pre=True)
+        check(C[rows], ref, z, "%dx%dx%d rows" % (M, N, K))
+
+
+# ---------------------------------------------------------------------------- the five workloads
+
+@pytest.mark.parametrize("name", ["square1024", "ragged2000x3000x1000", "skinny_decode"])
+def test_workload_full(name):
+    w = WORKLOADS[name]
+    parity(w.M, w.N, w.K, w.alpha, b_scaled=w.b_std_inv_sqrt_k)
+
+
+@pytest.mark.parametrize("name", ["square8192", "llm_mlp_up"])
+def test_workload_sampled_rows(name):
+    # Too big for the oracle in full: a seeded sample of 128 whole rows plus the tile edges.
+    w = WORKLOADS[name]
+    parity(w.M, w.N, w.K, w.alpha, b_scaled=w.b_std_inv_sqrt_k, rows=sample_rows(w.M))
+
+
+def test_page_instance_against_torch_reference():
+    # The tutorial's own check: seed 0, 1024^3, scale 0.5, against relu((a @ b) * scale)
+    # with rtol = atol = 1e-2.  A test-only cross-check; the oracle is the authority.
+    A, B = make_inputs(1024, 1024, 1024, seed=0)
+    C = run_gpu(A, B, 0.5)
+    ref = torch.relu((A.cuda() @ B.cuda()) * 0.5).cpu()
+    torch.testing.assert_close(C, ref, rtol=1e-2, atol=1e-2)
+
+
+# ---------------------------------------------------------------------------- tile edges
+
+EDGE_SHAPES = [
+    (1, 8, 8), (1, 64, 64), (7, 136, 72), (16, 128, 64), (17, 264, 1000), (33, 8, 16),
+    (64, 512, 56), (65, 256, 64), (127, 128, 64), (128, 256, 64), (129, 264, 72),
+    (255, 120, 200), (256, 256, 128), (257, 392, 136), (300, 8, 8), (1000, 1000, 8),
+    (130, 6144, 64), (384, 512, 1024),
+]
+
+
+@pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
+def test_edges_auto(M, N, K):
+    parity(M, N, K, 0.5, seed=M + N + K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (129, 264, 72), (255, 120, 200), (257, 392, 136),
+                                   (16, 16384, 1024), (640, 768, 4096)])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128])
+def test_edges_both_tile_widths(M, N, K, path):
+    parity(M, N, K, 1.0, path=path, seed=7 * M + N + K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (5, 40, 8), (16, 128, 64), (16, 136, 72),
+                                   (17, 1000, 1000), (32, 4096, 4096), (33, 264, 1024),
+                                   (48, 2048, 8192), (64, 640, 64), (64, 16384, 2048),
+                                   (3, 8, 100000 - 100000 % 8)])
+def test_small_m_path(M, N, K):
+    assert gsr.select_path(M, N, K) == 1
+    parity(M, N, K, 0.75, path=gsr.PATH_SKINNY, seed=M * N + K, b_scaled=True)
+
+
+def test_skinny_workload_through_tiled_path():
+    w = WORKLOADS["skinny_decode"]
+    parity(w.M, w.N, w.K, w.alpha, path=gsr.PATH_TILED, b_scaled=True)
+
+
+# ---------------------------------------------------------------------------- structure
+
+@pytest.mark.parametrize("M,K,path", [(64, 64, gsr.PATH_AUTO), (130, 72, gsr.PATH_AUTO),
+                                      (300, 256, gsr.PATH_TILED_128), (40, 136, gsr.PATH_SKINNY)])
+def test_identity_b_is_exact(M, K, path):
+    # the sum has one non-zero term, so fp32 accumulation is exact and C must equal the
+    # oracle bit for bit
+    A, _ = make_inputs(M, 8, K, seed=3)
+    B = torch.eye(K, dtype=torch.float16)
+    C = run_gpu(A, B, 0.5, path)
+    ref = oracle.gemm_scale_relu(A, B, 0.5)
+    assert np.array_equal(C.numpy().view(np.uint16), ref.view(np.uint16))
+
+
+@pytest.mark.parametrize("M,N,K,alpha,path", [(200, 264, 1000, 0.5, gsr.PATH_AUTO),
+                                              (8, 64, 3000, 1.0, gsr.PATH_SKINNY),
+                                              (130, 128, 2048, 1.0, gsr.PATH_TILED_256)])
+def test_all_ones_is_exact(M, N, K, alpha, path):
+    A = torch.ones(M, K, dtype=torch.float16)
+    B = torch.ones(K, N, dtype=torch.float16)
+    C = run_gpu(A, B, alpha, path)
+    assert torch.all(C == float(np.float16(alpha * K)))
+
+
+@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_SKINNY])
+def test_one_hot_rows(path):
+    M, N, K = 48, 392, 320
+    rng = np.random.default_rng(4)
+    ks = rng.integers(0, K, M)
+    A = torch.zeros(M, K, dtype=torch.float16)
+    A[torch.arange(M), torch.from_numpy(ks)] = 1
+    _, B = make_inputs(8, N, K, seed=5)
+    C = run_gpu(A, B, 1.0, path)
+    ref = oracle.gemm_scale_relu(A, B, 1.0)
+    assert np.array_equal(C.numpy().view(np.uint16), ref.view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [16, 300])
+def test_negative_alpha_nonnegative_inputs(M):
+    A, B = make_inputs(M, 520, 264, seed=6)
+    C = run_gpu(A.abs(), B.abs(), -0.5)
+    assert torch.all(C == 0)
+
+
+def test_k_zero_writes_zeros():
+    dC = torch.full((33, 64), float("nan"), dtype=torch.float16, device="cuda")
+    dA = torch.empty(33, 0, dtype=torch.float16, device="cuda")
+    dB = torch.empty(0, 64, dtype=torch.float16, device="cuda")
+    gsr.gemm_scale_relu(dA, dB, dC, 0.5)
+    torch.cuda.synchronize()
+    assert torch.all(dC == 0)
+
+
+def test_empty_output_leaves_buffers_alone():
+    dA = torch.ones(0, 64, dtype=torch.float16, device="cuda")
+    dB = torch.ones(64, 8, dtype=torch.float16, device="cuda")
+    dC = torch.empty(0, 8, dtype=torch.float16, device="cuda")
+    gsr.gemm_scale_relu(dA, dB, dC, 0.5)
+    torch.cuda.synchronize()
+
+
+def test_repeated_calls_are_deterministic():
+    for M in (16, 512):
+        A, B = make_inputs(M, 2048, 4096, seed=9)
+        c1 = run_gpu(A, B, 0.5)
+        c2 = run_gpu(A, B, 0.5)
+        assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+def test_streams_do_not_share_workspace():
+    # two small-M launches in flight on two streams at once; each must be correct
+    dev = torch.device("cuda", 0)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    A1, B1 = make_inputs(16, 4096, 8192, seed=11)
+    A2, B2 = make_inputs(24, 4096, 8192, seed=12)
+    d = [(A1.to(dev), B1.to(dev)), (A2.to(dev), B2.to(dev))]
+    outs = [torch.full((16, 4096), float("nan"), dtype=torch.float16, device=dev),
+            torch.full((24, 4096), float("nan"), dtype=torch.float16, device=dev)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (a, b), c, s in zip(d, outs, (s1, s2)):
+            with torch.cuda.stream(s):
+                gsr.gemm_scale_relu(a, b, c, 0.5, stream=s)
+    for s in (s1, s2):
+        assert gsr.device_status(s)[0] == gsr.Status.OK
+    for (A, B), c in zip(((A1, B1), (A2, B2)), outs):
+        ref, z = oracle.gemm_scale_relu(A, B, 0.5, return_pre=True)
+        check(c.cpu(), ref, z, "stream")
+
+
+def test_host_entry_point_round_trip():
+    M, N, K = 256, 384, 512
+    A, B = make_inputs(M, N, K, seed=13)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.empty(M, N, dtype=torch.float16).pin_memory()
+    dA = torch.empty(M, K, dtype=torch.float16, device="cuda")
+    dB = torch.empty(K, N, dtype=torch.float16, device="cuda")
+    dC = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    gsr.gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, 0.5)
+    torch.cuda.synchronize()
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, return_pre=True)
+    check(hC.clone(), ref, z, "host")
+
+
+def test_gpu_validation_codes():
+    dA = torch.empty(64, 64, dtype=torch.float16, device="cuda")
+    dB = torch.empty(64, 64, dtype=torch.float16, device="cuda")
+    assert gsr.gemm_scale_relu_ptr(dA.data_ptr(), dB.data_ptr(), dA.data_ptr(), 64, 64, 64, 1.0) \
+        == gsr.Status.ERR_ALIAS
+    assert gsr.gemm_scale_relu_ptr(dA.data_ptr() + 2, dB.data_ptr(), dB.data_ptr(), 8, 8, 8, 1.0) \
+        == gsr.Status.ERR_ALIGNMENT
