@@ -1,0 +1,412 @@
+"""Benchmark of the fused GEMM + scale + ReLU library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gsr|reference]
+
+One step = one call of gemm_scale_relu on the whole workload (A, B resident in HBM).
+Metric: TFLOP/s = 2*M*N*K / time, device-timed with CUDA events on the launching stream,
+as the tutorial's benchmark_op does ("Tutorial14: 使用TileLang语言编写attention算子",
+section 2: warm-up calls, CUDA events around back-to-back calls, 2*M*N*K / latency).
+
+Prints ONE JSON line (rank 0).  Besides the timing it carries:
+  roofline      the kernel's achieved TFLOP/s (or GB/s for the HBM-bound small-M shape)
+                against the measured peak in MEASURED_PEAKS.json, with the DRAM traffic
+                per launch from the committed ncu summary when it matches the current
+                kernel sources;
+  e2e           the same metric through gemm_scale_relu_host: pinned host A, B copied in
+                and C copied out inside the timed region, every step;
+  cpu_baseline  the fp64 CPU oracle timed on this host on a bounded sample of rows;
+  clocks        SM clocks and throttle reasons sampled by nvidia-smi during the run.
+With --impl reference the line times the oracle itself (the CPU reference arm).
+N > 1 (torchrun): every rank runs its own full copy of the workload (replicas, weak
+scaling); the time is the max over ranks and the value the sum of all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from tensor_core_gemm_multistage_gb300.workloads import WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "fused GEMM+scale+ReLU TFLOP/s and % of GB300 dense FP16 peak, 1 GPU"
+DEFAULT_WORKLOAD = "square8192"
+L2_BYTES = 126 * 1024 * 1024
+KERNEL_SOURCES = ["csrc/gemm_tiled.cu", "csrc/gemm_skinny.cu", "csrc/ptx.cuh",
+                  "csrc/device_common.cuh", "csrc/kernels.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "tensor_core_gemm_multistage_gb300")
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(pkg, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel sources; lines: `workload kernel sources_hash bytes_per_launch note...`."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    cur = kernel_source_hash()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload \
+                    and parts[1] == kernel and parts[2] == cur:
+                return float(parts[3])
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity at world size 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, timestamped on arrival."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str | None, interval_ms: int = 100):
+        self.uuid = uuid
+        self.samples = []
+        self.proc = None
+        self.interval_ms = interval_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        threading.Thread(target=self._read, daemon=True).start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), parts[4:9],
+                                     parts[0]))
+            except ValueError:
+                pass
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        mine = [s for s in self.samples if s[4] == self.uuid]
+        if not mine and self.samples:    # uuid not reported: the first GPU listed
+            first = self.samples[0][4]
+            mine = [s for s in self.samples if s[4] == first]
+        self.samples = mine
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if not inside:   # region shorter than the sampling interval: nearest samples under load
+            inside = [s for s in self.samples if t0 - 1.0 <= s[0] <= t1 + 0.5]
+            window = "around the timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "no samples"}
+        reasons = set()
+        for s in inside:
+            flags = s[3]
+            for name, flag in zip(self.REASONS, flags[1:5]):
+                if flag.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+def gpu_uuid():
+    try:
+        import torch
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def time_oracle(A, B, alpha, seconds: float):
+    """Run the oracle on chunks of whole rows of C (one row per host thread per chunk)
+    until about `seconds` have passed; returns (rows done, elapsed s, threads used)."""
+    import oracle
+    oracle.build()
+    M = A.shape[0]
+    threads = oracle.max_threads()
+    chunk = min(M, threads)
+    done, t_total, row = 0, 0.0, 0
+    while t_total < seconds:
+        rows = [(row + i) % M for i in range(chunk)]
+        t = time.perf_counter()
+        oracle.gemm_scale_relu(A, B, alpha, rows=rows)
+        t_total += time.perf_counter() - t
+        done += chunk
+        row = (row + chunk) % M
+    return done, t_total, chunk
+
+
+# ---------------------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+    import oracle
+    oracle.build()
+    A, B = workload_inputs(w)
+    # calibrate with one chunk (one row per host thread), then size each step as a whole
+    # number of chunks so that the --warmup + --steps run stays within about two minutes
+    threads = oracle.max_threads()
+    chunk = min(w.M, threads)
+    t = time.perf_counter()
+    oracle.gemm_scale_relu(A, B, w.alpha, rows=list(range(chunk)))
+    per_chunk = max(time.perf_counter() - t, 1e-6)
+    budget = 120.0
+    chunks = max(1, int(budget / ((args.steps + args.warmup) * per_chunk)))
+    rows_per_step = min(w.M, chunks * chunk)
+    row = 0
+    for _ in range(args.warmup):
+        oracle.gemm_scale_relu(A, B, w.alpha, rows=[(row + i) % w.M for i in range(rows_per_step)])
+        row += rows_per_step
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_scale_relu(A, B, w.alpha, rows=[(row + i) % w.M for i in range(rows_per_step)])
+        row += rows_per_step
+    elapsed = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    value = flops / elapsed / 1e12
+    sample = "%d of %d output rows (whole rows of C) per step" % (rows_per_step, w.M)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn, fp16)",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": min(threads, rows_per_step),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+            "inputs": "A,B fp16 from seeded randn" + (", B*K^-1/2" if w.b_std_inv_sqrt_k else ""),
+            "accumulate": "f32", "output": "f16",
+            "l2": ("inputs larger than L2 (A+B %d MiB > 126 MiB), no flush"
+                   % ((w.M * w.K + w.K * w.N) * 2 >> 20))
+            if (w.M * w.K + w.K * w.N) * 2 > L2_BYTES else "flush L2 between steps"}
+
+
+def run_gsr(args, w):
+    import torch
+
+    import tensor_core_gemm_multistage_gb300 as gsr
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gsr.build()
+
+    A, B = workload_inputs(w)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.empty(w.M, w.N, dtype=torch.float16, device=dev)
+    inputs_bytes = (w.M * w.K + w.K * w.N) * 2
+    flush = None
+    if inputs_bytes <= L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    path = gsr.select_path(w.M, w.N, w.K)
+    kernel = "gsr_skinny_kernel" if path == 1 else "gsr_tiled_kernel"
+
+    def step():
+        gsr.gemm_scale_relu(dA, dB, dC, w.alpha, stream=stream)
+
+    sampler = ClockSampler(gpu_uuid()).start() if rank == 0 else None
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    status, code = gsr.device_status(stream)
+    if status != gsr.Status.OK:
+        raise RuntimeError("device status %s code %#x" % (status.name, code))
+
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    region_ms = start.elapsed_time(stop)
+    step_ms = region_ms / args.steps if flush is None else sum(kernel_ms) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    kernel_avg_ms = max_over_ranks(sum(kernel_ms) / len(kernel_ms), world)
+
+    # end-to-end through the host entry point: pinned host in, pinned host out
+    e2e = None
+    if args.e2e_steps > 0:
+        hA, hB = A.pin_memory(), B.pin_memory()
+        hC = torch.empty(w.M, w.N, dtype=torch.float16).pin_memory()
+        gsr.gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, w.alpha, stream=stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            gsr.gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, w.alpha, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world)
+        e2e = {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": inputs_bytes, "d2h_bytes_per_step": w.M * w.N * 2,
+               "ms_per_step": e2e_ms, "steps": args.e2e_steps}
+    if sampler is not None:
+        sampler.stop()
+
+    if rank != 0:
+        return 0
+
+    peaks, peaks_src = measured_peaks()
+    value = world * w.flops / (step_ms * 1e-3) / 1e12
+    if path == 1:
+        achieved = w.bytes / (kernel_avg_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "kernel": kernel,
+                    "per_launch": "%d algorithmic bytes (A+B read once, C written once)" % w.bytes}
+    else:
+        achieved = w.flops / (kernel_avg_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "kernel": kernel,
+                    "per_launch": "%d algorithmic flops (2*M*N*K)" % w.flops}
+    roofline["traffic"] = read_traffic(w.name, kernel)
+    roofline["peak_source"] = ("%s: %s; fp16 dense rate taken equal to the bf16 rate "
+                               "(nominal ratio 1)" % (peaks_src, "hbm_gbs" if path == 1
+                                                      else "bf16_tflops burst"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded randn, fp16)", "config": config_of(w),
+        "roofline": roofline,
+        "kernel_ms": kernel_avg_ms,
+        "gpu_launches": args.steps,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if sampler is not None:
+        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+    if world == 1 and args.cpu_seconds > 0:
+        rows, secs, cores = time_oracle(A, B, w.alpha, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": 2.0 * rows * w.N * w.K / secs / 1e12, "unit": "TFLOP/s",
+                                "cores": cores, "kind": "oracle",
+                                "sample": "%d whole rows of C (of %d), %.1f s" % (rows, w.M, secs)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gsr", "reference"], default="gsr")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gsr(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
