@@ -43,7 +43,10 @@ typedef enum gsr_status {
     /* A kernel gave up on a bounded wait (reported by gsr_device_status). */
     GSR_ERR_DEVICE_TIMEOUT = 5,
     /* The current device is not compute capability 10.3 (GB300). */
-    GSR_ERR_UNSUPPORTED_DEVICE = 6
+    GSR_ERR_UNSUPPORTED_DEVICE = 6,
+    /* gemm_scale_relu_noalloc: these sizes need more scratch than its fixed
+     * array holds. */
+    GSR_ERR_SCRATCH_LIMIT = 7
 } gsr_status;
 
 /*
@@ -88,6 +91,37 @@ gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int
 gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* dA, void* dB,
                                 void* dC, int64_t M, int64_t N, int64_t K, float alpha,
                                 struct CUstream_st* stream);
+
+/*
+ * gemm_scale_relu without any device-memory allocation, for callers that cannot
+ * let a library allocate: for example a serving runtime that plans all of its
+ * device memory at start-up and forbids allocations afterwards, or a
+ * latency-critical loop that cannot take the implicit synchronisation of a
+ * first-time cudaMalloc.  (No counterpart on the pages: they allocate through
+ * the TileLang JIT and PyTorch.)
+ *
+ * Arguments, layout, ownership and result are those of gemm_scale_relu, for
+ * the small-M kernel only: 1 <= M <= 64 (M > 64 returns GSR_ERR_INVALID_ARG;
+ * M == 0 or N == 0 is a no-op and K == 0 clears C, as there).  The caller
+ * passes A, B and C; the kernel's scratch (error word, per-tile tickets and
+ * split-K partial tiles) lives in one fixed 12 MiB array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * Sizes whose scratch would not fit return GSR_ERR_SCRATCH_LIMIT before any
+ * work is queued; on a 152-SM GB300 that happens only for N above about
+ * 8.3e7 (33 <= M <= 64), 2.4e8 (17 <= M <= 32) or 3.2e8 (M <= 16).
+ * The call never runs cudaMalloc, cudaFree or any other allocating routine.
+ *
+ * The first call on a device looks up the array's device address (one-time
+ * set-up with that device current); make that first call before any stream
+ * capture.  Every call shares the array and it keeps the last call's
+ * contents; each call clears the parts that must start at zero, on `stream`,
+ * before its kernel.  Calls whose work overlaps on the GPU (for example on two
+ * streams with no ordering between them) race on the array and produce wrong
+ * results: order them on one stream.  A bounded-wait timeout inside this
+ * variant is not reported through gsr_device_status.
+ */
+gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                   int64_t K, float alpha, struct CUstream_st* stream);
 
 /*
  * Waits for `stream`, then reads and clears the error word of the (current

@@ -24,6 +24,7 @@ class Status(enum.IntEnum):
     ERR_CUDA = 4
     ERR_DEVICE_TIMEOUT = 5
     ERR_UNSUPPORTED_DEVICE = 6
+    ERR_SCRATCH_LIMIT = 7
 
 
 class GsrError(RuntimeError):
@@ -61,6 +62,8 @@ def lib() -> ctypes.CDLL:
                                        ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int)
         L.gemm_scale_relu.restype = i32
         L.gemm_scale_relu.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
+        L.gemm_scale_relu_noalloc.restype = i32
+        L.gemm_scale_relu_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
         L.gemm_scale_relu_host.restype = i32
         L.gemm_scale_relu_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, vp]
         L.gsr_device_status.restype = i32

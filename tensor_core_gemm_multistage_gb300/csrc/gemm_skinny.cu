@@ -325,3 +325,78 @@ cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, cons
 }
 
 }  // namespace gsr
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the small-M launch.
+//
+// Some callers cannot let a library call cudaMalloc: a serving runtime that plans all of
+// its device memory at start-up and forbids allocations afterwards, or a latency-critical
+// loop where the implicit synchronisation of a first-time cudaMalloc is not acceptable.
+// For them, gemm_scale_relu_noalloc runs the same small-M kernel with its scratch (error
+// word, per-tile tickets, split-K partial tiles) carved out of the fixed array below
+// instead of a library-allocated workspace.  The array is a module global, so every GPU
+// that loads this library holds its 12 MiB until the process exits.
+//
+// Every call on a device shares the one array and it keeps whatever the last call left in
+// it: the error word and the tickets, which must start at zero, are cleared on the stream
+// at the start of each call; the partial tiles are always written before they are read.
+// Two calls whose kernels overlap on the GPU (different streams, no ordering between them)
+// race on the array and give wrong results.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)12 << 20;
+constexpr int kNoAllocMaxDevices = 64;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_gsr_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace gsr {
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+// Byte layout inside the array: [0, 256) error word, [256, 256 + tickets) tickets rounded up
+// to 256 bytes, then the partial tiles.
+size_t noalloc_scratch_need(int num_ctas, int n_tiles, int mp) {
+    const size_t tickets = ((size_t)n_tiles * sizeof(int) + 255) / 256 * 256;
+    return 256 + tickets + (size_t)num_ctas * 2 * mp * 128 * sizeof(float);
+}
+
+cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tmAt, SkinnyParams p,
+                                  int mp, cudaStream_t stream) {
+    // Set-up, once per device and with that device current: the device address of the
+    // array.  (In host code the array's name is only a host-side stand-in.)
+    static std::mutex mu;
+    static void* base_of[kNoAllocMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!base_of[dev]) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_gsr_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            base_of[dev] = ptr;
+        }
+        base = base_of[dev];
+    }
+    if (noalloc_scratch_need(p.num_ctas, p.num_n_tiles, mp) > kNoAllocScratchBytes)
+        return cudaErrorInvalidValue;
+    unsigned char* b = static_cast<unsigned char*>(base);
+    const size_t tickets = ((size_t)p.num_n_tiles * sizeof(int) + 255) / 256 * 256;
+    p.err = reinterpret_cast<int*>(b);
+    p.tickets = reinterpret_cast<int*>(b + 256);
+    p.partials = reinterpret_cast<float*>(b + 256 + tickets);
+    e = cudaMemsetAsync(b, 0, 256 + tickets, stream);   // error word and tickets start at 0
+    if (e != cudaSuccess) return e;
+    if (mp == 16) return launch_cfg<Sk16>(tmBt, tmAt, p, stream);
+    if (mp == 32) return launch_cfg<Sk32>(tmBt, tmAt, p, stream);
+    if (mp == 64) return launch_cfg<Sk64>(tmBt, tmAt, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gsr

@@ -305,6 +305,58 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
     return GSR_OK;
 }
 
+// No device-memory allocation anywhere on this path: plain attribute queries instead of
+// the cached device table, the small-M kernel with its scratch in the library's fixed
+// array (gemm_skinny.cu).
+gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                   int64_t K, float alpha, CUstream_st* stream) {
+    bool nothing = false;
+    gsr_status s = validate(A, B, C, M, N, K, &nothing);
+    if (s != GSR_OK || nothing) return s;
+    if (M > kSkinnyMaxM) return GSR_ERR_INVALID_ARG;
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e);
+    if (major != 10 || minor != 3) return GSR_ERR_UNSUPPORTED_DEVICE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    const int n_tiles = (int)((N + 127) / 128);
+    const int kbpt = (int)((K + 63) / 64);
+    const long long T = (long long)n_tiles * (kbpt > 0 ? kbpt : 1);
+    const int P = (int)(T < sms ? T : sms);
+    if (gsr::noalloc_scratch_need(P, n_tiles, mp) > gsr::noalloc_scratch_bytes())
+        return GSR_ERR_SCRATCH_LIMIT;
+    if (K == 0) {
+        e = cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
+        return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+    }
+    if ((s = load_encoder()) != GSR_OK) return s;
+    CUtensorMap tmBt, tmAt;
+    if ((s = encode_fp16_2d(&tmBt, B, K, N, 64, 64)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmAt, A, M, K, 64, mp)) != GSR_OK) return s;
+    gsr::SkinnyParams p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.alpha = alpha;
+    p.num_n_tiles = n_tiles;
+    p.num_k_blocks = kbpt;
+    p.total_units = T;
+    p.num_ctas = P;
+    p.partials = nullptr;   // filled from the fixed array by the launch
+    p.tickets = nullptr;
+    p.err = nullptr;
+    p.C = static_cast<__half*>(C);
+    p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    p.test_flags = 0;
+    e = gsr::launch_skinny_noalloc(tmBt, tmAt, p, mp, st);
+    return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+}
+
 gsr_status gsr_device_status(CUstream_st* stream, int* code) {
     if (code) *code = 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -356,6 +408,7 @@ const char* gsr_status_string(gsr_status s) {
         case GSR_ERR_CUDA: return "GSR_ERR_CUDA";
         case GSR_ERR_DEVICE_TIMEOUT: return "GSR_ERR_DEVICE_TIMEOUT";
         case GSR_ERR_UNSUPPORTED_DEVICE: return "GSR_ERR_UNSUPPORTED_DEVICE";
+        case GSR_ERR_SCRATCH_LIMIT: return "GSR_ERR_SCRATCH_LIMIT";
     }
     return "GSR_ERR_UNKNOWN";
 }

@@ -61,6 +61,14 @@ cudaError_t launch_tiled(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
 cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
                           int mp, cudaStream_t stream);
 
+// Allocation-free small-M launch: scratch comes from a fixed module array of
+// noalloc_scratch_bytes() bytes (see gemm_skinny.cu); p.partials, p.tickets and p.err are
+// filled in by the call.  noalloc_scratch_need() is the byte count a launch uses.
+cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tmAt, SkinnyParams p,
+                                  int mp, cudaStream_t stream);
+size_t noalloc_scratch_bytes();
+size_t noalloc_scratch_need(int num_ctas, int n_tiles, int mp);
+
 // Shared-memory bytes a launch needs (for the one-time attribute set-up).
 int tiled_smem_bytes(int bn);
 int skinny_smem_bytes(int mp);
