@@ -1,0 +1,62 @@
+"""Failure detection without a GPU fault.
+
+Every wait inside the kernels is bounded.  A test-only flag makes the first CTA's TMA
+producer skip its first shared-memory fill, so that CTA's MMA issuer waits for data that
+never comes.  With a short limit the wait runs out, the kernel records a code in the
+stream's error word, drains what it started, frees its tensor memory and exits; the host
+reads GSR_ERR_DEVICE_TIMEOUT from gsr_device_status.  Nothing traps, and a normal call
+right after must still be correct (same context, small-M tickets reset).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tensor_core_gemm_multistage_gb300 as gsr
+from tensor_core_gemm_multistage_gb300.workloads import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gsr.build()
+    oracle.build()
+    yield
+    gsr.set_test_flags(0)
+    gsr.set_wait_timeout_ns(1_000_000_000)
+    gsr.set_path_override(gsr.PATH_AUTO)
+
+
+@pytest.mark.parametrize("M,N,K,path,kernel", [(512, 1024, 1024, gsr.PATH_TILED, 0x100),
+                                               (16, 4096, 8192, gsr.PATH_SKINNY, 0x200)])
+def test_timeout_is_reported_and_the_gpu_stays_usable(M, N, K, path, kernel):
+    dev = torch.device("cuda", 0)
+    A, B = make_inputs(M, N, K, seed=21)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.zeros(M, N, dtype=torch.float16, device=dev)
+    gsr.set_path_override(path)
+    gsr.set_wait_timeout_ns(50_000_000)        # 50 ms
+    gsr.set_test_flags(1)
+    try:
+        gsr.gemm_scale_relu(dA, dB, dC, 0.5)
+        status, code = gsr.device_status()
+    finally:
+        gsr.set_test_flags(0)
+        gsr.set_wait_timeout_ns(1_000_000_000)
+    assert status == gsr.Status.ERR_DEVICE_TIMEOUT
+    assert code & 0xF00 == kernel and (code & 0xFF) in (1, 2, 3, 4, 5)
+    # the error word was cleared by the read
+    assert gsr.device_status() == (gsr.Status.OK, 0)
+
+    # same process, same context: a normal call is correct again
+    dC.fill_(float("nan"))
+    try:
+        gsr.gemm_scale_relu(dA, dB, dC, 0.5)
+        status, code = gsr.device_status()
+    finally:
+        gsr.set_path_override(gsr.PATH_AUTO)
+    assert status == gsr.Status.OK, hex(code)
+    ref = oracle.gemm_scale_relu(A, B, 0.5).astype(np.float64)
+    got = dC.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
