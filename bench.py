@@ -41,8 +41,9 @@ from tensor_core_gemm_multistage_gb300.workloads import WORKLOADS, workload_inpu
 METRIC = "fused GEMM+scale+ReLU TFLOP/s and % of GB300 dense FP16 peak, 1 GPU"
 DEFAULT_WORKLOAD = "square8192"
 L2_BYTES = 126 * 1024 * 1024
-KERNEL_SOURCES = ["csrc/gemm_tiled.cu", "csrc/gemm_skinny.cu", "csrc/ptx.cuh",
-                  "csrc/device_common.cuh", "csrc/kernels.h"]
+KERNEL_SOURCES = ["csrc/gemm_tiled.cu", "csrc/gemm_pair.cu", "csrc/gemm_skinny.cu",
+                  "csrc/ptx.cuh", "csrc/device_common.cuh", "csrc/kernels.h"]
+KERNEL_NAMES = {0: "gsr_tiled_kernel", 1: "gsr_skinny_kernel", 2: "gsr_pair_kernel"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -282,7 +283,7 @@ def run_gsr(args, w):
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     path = gsr.select_path(w.M, w.N, w.K)
-    kernel = "gsr_skinny_kernel" if path == 1 else "gsr_tiled_kernel"
+    kernel = KERNEL_NAMES[path]
 
     def step():
         gsr.gemm_scale_relu(dA, dB, dC, w.alpha, stream=stream)

@@ -67,7 +67,8 @@ typedef enum gsr_status {
  * K == 0: C is filled with zeros (ReLU(alpha * 0)).
  *
  * Paths: M <= 64 runs the small-M kernel (B streamed once, K split across
- * SMs), otherwise the tiled kernel.
+ * SMs); larger M runs a tiled kernel, on CTA pairs with 256 x 256 tiles when
+ * there are enough of them to fill the GPU, else one CTA per 128-row tile.
  *
  * Device memory the library owns: on the first call on each (device, stream)
  * pair it allocates a 4-byte error word for that stream, and the small-M
@@ -136,12 +137,15 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
  */
 gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
 
-/* Path the library would take for these sizes: 0 = tiled, 1 = small-M. */
+/* Kernel the library would run for these sizes on the current device: 0 = tiled
+ * (one CTA per 128-row tile), 1 = small-M, 2 = tiled on CTA pairs (256 x 256
+ * tiles; chosen when there is at least one full wave of such tiles). */
 int gsr_select_path(int64_t M, int64_t N, int64_t K);
 
 /* Forces a path for later calls (process-wide): 0 = automatic (default),
  * 1 = tiled with automatic tile width, 2 = small-M (only honoured when
- * M <= 64), 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles.
+ * M <= 64), 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles,
+ * 5 = tiled on CTA pairs with 256 x 256 tiles.
  * For tests and measurements. */
 void gsr_set_path_override(int path);
 

@@ -5,7 +5,8 @@ sources in ``csrc/`` for sm_103a; this package holds its ctypes binding and the 
 input generators.  Operator: "Tutorial14: 使用TileLang语言编写attention算子", sections 2
 and 3.
 """
-from .binding import (PATH_AUTO, PATH_SKINNY, PATH_TILED, PATH_TILED_128, PATH_TILED_256,
+from .binding import (KERNEL_PAIR, KERNEL_SKINNY, KERNEL_TILED, PATH_AUTO, PATH_PAIR,
+                      PATH_SKINNY, PATH_TILED, PATH_TILED_128, PATH_TILED_256,
                       GsrError, Status, device_status, gemm_scale_relu, gemm_scale_relu_host,
                       gemm_scale_relu_host_ptr, gemm_scale_relu_ptr, last_cuda_error, lib,
                       library_path, select_path, set_path_override, set_test_flags,
@@ -13,7 +14,7 @@ from .binding import (PATH_AUTO, PATH_SKINNY, PATH_TILED, PATH_TILED_128, PATH_T
 from ._build import build
 
 __all__ = [
-    "PATH_AUTO", "PATH_SKINNY", "PATH_TILED", "PATH_TILED_128", "PATH_TILED_256", "GsrError",
+    "KERNEL_PAIR", "KERNEL_SKINNY", "KERNEL_TILED", "PATH_AUTO", "PATH_PAIR", "PATH_SKINNY", "PATH_TILED", "PATH_TILED_128", "PATH_TILED_256", "GsrError",
     "Status", "build", "device_status", "gemm_scale_relu", "gemm_scale_relu_host",
     "gemm_scale_relu_host_ptr", "gemm_scale_relu_ptr", "last_cuda_error", "lib", "library_path",
     "select_path", "set_path_override", "set_test_flags", "set_wait_timeout_ns", "shutdown",

@@ -1,0 +1,338 @@
+// gemm_pair.cu - tiled path of C = ReLU(alpha * A.B) on CTA pairs (sm_103a, cta_group::2).
+//
+// Same operator and epilogue as gemm_tiled.cu ("Tutorial14: 使用TileLang语言编写attention算子",
+// section 2 kernel and section 3 formula / tiling / fused epilogue); what changes is how a
+// 256 x 256 output tile is shared by the two CTAs (two SMs) of a cluster:
+//  * CTA r of the pair loads rows [m0 + 128r, +128) of A and columns [n0 + 128r, +128) of B
+//    into its own shared memory, at the same offsets in both CTAs;
+//  * one thread of the leader CTA (rank 0) issues tcgen05.mma.cta_group::2 with M = 256,
+//    N = 256: the tensor cores of both SMs read both CTAs' A rows and B columns, and each
+//    CTA's TMEM receives its 128 rows x 256 columns of the accumulator;
+//  * both CTAs' TMA loads count their bytes on the leader's "full" barrier (the leader
+//    arms it with the pair's total); the MMA's commits arrive on the "empty" and
+//    "accumulator full" barriers of both CTAs at once (multicast); both CTAs' epilogue
+//    warps arrive on the leader's "accumulator empty" barrier.
+// Each SM thus moves half of B through its shared memory instead of all of it: per k-block
+// an SM stages 32 KB (not 48 KB) and its tensor core reads 32 KB (not 48 KB) of operands
+// for the same 128 x 256 x 64 of work, which is what limited the single-CTA kernel.
+#include <atomic>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace gsr {
+namespace {
+
+struct PairCfg {
+    static constexpr int BM = 256, BN = 256, BK = 64, STAGES = 6;
+    static constexpr int HALF_M = 128, HALF_N = 128;          // per CTA
+    static constexpr int NUM_THREADS = 192;
+    static constexpr int A_STAGE_BYTES = HALF_M * BK * 2;     // 16 KB
+    static constexpr int B_CHUNK_BYTES = BK * 64 * 2;         // 8 KB box (64 columns)
+    static constexpr int B_STAGE_BYTES = BK * HALF_N * 2;     // 16 KB
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;   // per CTA
+    static constexpr int C_BUF_BYTES = HALF_M * 64 * 2;       // 16 KB staging chunk
+    static constexpr int C_BUFS = 2;
+    static constexpr int TMEM_COLS = 2 * BN;                  // two accumulators of 256 columns
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+    static constexpr int OFF_C = OFF_B + STAGES * B_STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_C + C_BUFS * C_BUF_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+    static constexpr uint32_t TEMPTY_ARRIVALS = 8;            // 4 epilogue warps x 2 CTAs
+    static constexpr uint64_t ABORT_GUARD_NS = 2000000;       // see the producer's exit
+
+    static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
+};
+
+__device__ __forceinline__ void pair_tile_coords(int t, int num_m_blocks, int num_n_blocks,
+                                                 int group_m, int& mb, int& nb) {
+    const int per_group = group_m * num_n_blocks;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int gsz = min(num_m_blocks - first_m, group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % gsz;
+    nb = r / gsz;
+}
+
+__global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
+    gsr_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const TiledParams p) {
+    using Cfg = PairCfg;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+
+    auto full_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (S + s); };
+    auto tfull_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + a); };
+    auto tempty_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * S + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();          // 0: leader, 1: peer
+    const int cluster = (int)cluster_id_x();
+    const int nclusters = (int)cluster_count_x();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);                // leader: its arrive.expect_tx (pair bytes)
+            mbar_init(empty_bar(s), 1);               // multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);               // multicast commit
+            mbar_init(tempty_bar(a), Cfg::TEMPTY_ARRIVALS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish_alloc_permit_pair();
+    }
+    tcgen05_fence_before();
+    cluster_sync();                                   // barriers of both CTAs exist from here on
+    tcgen05_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const Waiter w{p.err, p.timeout_ns, abort_flag, kDevErrKernelTiled};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (both CTAs)
+        const uint64_t pol = l2_policy_evict_last();
+        uint32_t stage = 0, phase = 0;
+        uint32_t armed_mask = 0, armed_parity = 0;
+        bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+        bool ok = true;
+        for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
+            int mb, nb;
+            pair_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+            const int m_row = mb * Cfg::BM + (int)rank * Cfg::HALF_M;
+            const int n_col = nb * Cfg::BN + (int)rank * Cfg::HALF_N;
+            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                bool got = true;
+                if (lane == 0) got = w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty);
+                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                if (lane == 0) {
+                    if (drop_first) {
+                        drop_first = false;
+                    } else {
+                        const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
+                        if (rank == 0) {
+                            mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+                            armed_mask |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        tma_load_2d_pair(sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES, &tmA,
+                                         leader_full, kb * Cfg::BK, m_row, pol);
+#pragma unroll
+                        for (int j = 0; j < Cfg::HALF_N / 64; ++j)
+                            tma_load_2d_pair(sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES +
+                                                 j * Cfg::B_CHUNK_BYTES,
+                                             &tmB, leader_full, n_col + j * 64, kb * Cfg::BK, pol);
+                    }
+                }
+                __syncwarp();
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (lane == 0) {
+            // Leader: every stage it armed completes only once both CTAs' bytes landed.
+            for (int s = 0; s < S; ++s)
+                if (armed_mask & (1u << s)) w.drain(full_bar(s), (armed_parity >> s) & 1u);
+            // After an abort the peer cannot observe its own copies (they count on the
+            // leader's barrier); they depend on nothing and land within microseconds, so it
+            // waits a fixed guard time before it may leave.
+            if (!ok) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < Cfg::ABORT_GUARD_NS) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader)
+        if (rank == 0) {
+            uint32_t stage = 0, phase = 0, it = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters, ++it) {
+                const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
+                bool got = true;
+                if (lane == 0) got = w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty);
+                if (!__shfl_sync(0xffffffffu, got, 0)) break;
+                tcgen05_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * Cfg::BN;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (lane == 0) got = w.wait(full_bar(stage), phase, kDevErrMmaFull);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                    tcgen05_fence_after();
+                    if (lane == 0) {
+                        const uint32_t a0 = sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES;
+                        const uint32_t b0 = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
+#pragma unroll
+                        for (int k = 0; k < Cfg::BK / 16; ++k) {
+                            const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(b0 + k * 2048, Cfg::B_CHUNK_BYTES, 1024);
+                            mma_f16_ss_pair(d_tmem, ad, bd, Cfg::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit_pair(empty_bar(stage), 0x3);   // frees the stage in both CTAs
+                    }
+                    __syncwarp();
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if (lane == 0) mma_commit_pair(tfull_bar(acc), 0x3);   // both halves of D ready
+                __syncwarp();
+            }
+            if (lane == 0) {
+                mma_commit_pair(drain_bar, 0x1);
+                w.drain(drain_bar, 0);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int et = threadIdx.x - 64;
+        uint32_t it = 0, cidx = 0;
+        for (int tile = cluster; tile < p.num_tiles; tile += nclusters, ++it) {
+            const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
+            const bool got = w.wait(tfull_bar(acc), acc_parity, kDevErrEpilogueFull);
+            if (!named_bar_and(1, 128, got)) break;
+            tcgen05_fence_after();
+            int mb, nb;
+            pair_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+            const int m0 = mb * Cfg::BM + (int)rank * Cfg::HALF_M;   // this CTA's rows
+            const int n0 = nb * Cfg::BN;
+            const int nchunks = (m0 < p.M) ? (min(Cfg::BN, p.N - n0) + 63) / 64 : 0;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * Cfg::BN;
+            const uint32_t leader_tempty = map_to_cta(tempty_bar(acc), 0);
+            if (nchunks == 0) {
+                // nothing of this half-tile lies inside C; still release the accumulator
+                tcgen05_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_tempty);
+            }
+            for (int c = 0; c < nchunks; ++c) {
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(t_row + c * 64, r0);
+                tmem_ld_32x32b_x32(t_row + c * 64 + 32, r1);
+                tmem_ld_wait(r0);
+                tmem_ld_wait(r1);
+                if (c == nchunks - 1) {
+                    tcgen05_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(leader_tempty);
+                }
+                const uint32_t buf = cidx & 1u;
+                if (et == 0) bulk_wait_group_read<1>();
+                named_bar_sync(1, 128);
+                uint8_t* crow = smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES + row * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t* src = (j < 4) ? (r0 + 8 * j) : (r1 + 8 * (j - 4));
+                    uint4 v;
+                    v.x = scale_relu_pack(src[0], src[1], p.alpha);
+                    v.y = scale_relu_pack(src[2], src[3], p.alpha);
+                    v.z = scale_relu_pack(src[4], src[5], p.alpha);
+                    v.w = scale_relu_pack(src[6], src[7], p.alpha);
+                    *reinterpret_cast<uint4*>(crow + ((j ^ (row & 7)) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (et == 0) {
+                    tma_store_2d(&tmC, sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, n0 + c * 64, m0);
+                    bulk_commit_group();
+                }
+                ++cidx;
+            }
+        }
+        if (et == 0) bulk_wait_group<0>();
+    }
+
+    // Neither CTA may leave (or free TMEM) while the pair still uses its shared memory,
+    // barriers or tensor memory.
+    tcgen05_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        tcgen05_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+int pair_smem_bytes() { return PairCfg::SMEM_BYTES; }
+
+// Largest number of co-resident CTA pairs, per device (0 if the query fails).
+int pair_max_active_clusters() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaFuncSetAttribute(gsr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairCfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(PairCfg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gsr_pair_kernel, &cfg) != cudaSuccess) return 0;
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const TiledParams& p, int clusters, cudaStream_t stream) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(gsr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairCfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(PairCfg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gsr_pair_kernel, tmA, tmB, tmC, p);
+}
+
+}  // namespace gsr

@@ -183,12 +183,19 @@ gsr_status stream_state(int dev, cudaStream_t stream, size_t need_partials, size
     return GSR_OK;
 }
 
-int choose_path(int64_t M) {
+// 0: tiled, one CTA per 128 x BN tile; 1: small-M; 2: tiled on CTA pairs (256 x 256 tiles),
+// taken when there are at least as many pair tiles as half the SMs (one full wave of pairs).
+int choose_path(int64_t M, int64_t N, int num_sms) {
     const int o = g_path_override.load(std::memory_order_relaxed);
     if (o == 1 || o == 3 || o == 4) return 0;
+    if (o == 5) return 2;
     if (o == 2 && M <= kSkinnyMaxM) return 1;
-    return M <= kSkinnyMaxM ? 1 : 0;
+    if (M <= kSkinnyMaxM) return 1;
+    const long long pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    return pair_tiles >= num_sms / 2 ? 2 : 0;
 }
+
+constexpr int kDefaultSms = 152;   // for gsr_select_path before any device is touched
 
 gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
                      cudaStream_t stream, int dev, const DeviceInfo& info) {
@@ -223,6 +230,35 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
     const int grid = p.num_tiles < info.num_sms ? p.num_tiles : info.num_sms;
     cudaError_t e = gsr::launch_tiled(tmA, tmB, tmC, p, bn, grid, stream);
+    return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+}
+
+gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
+                    cudaStream_t stream, int dev, const DeviceInfo& info) {
+    StreamState st;
+    gsr_status s = stream_state(dev, stream, 0, 0, &st);
+    if (s != GSR_OK) return s;
+    CUtensorMap tmA, tmB, tmC;
+    if ((s = encode_fp16_2d(&tmA, A, M, K, 64, 128)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmC, C, M, N, 64, 128)) != GSR_OK) return s;
+    gsr::TiledParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.num_m_blocks = (M + 255) / 256;
+    p.num_n_blocks = (N + 255) / 256;
+    p.num_k_blocks = (K + 63) / 64;
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.group_m = kGroupM / 2;
+    p.err = st.err;
+    p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    p.test_flags = g_test_flags.load(std::memory_order_relaxed);
+    int clusters = gsr::pair_max_active_clusters();
+    if (clusters <= 0) clusters = info.num_sms / 2;
+    if (clusters > p.num_tiles) clusters = p.num_tiles;
+    cudaError_t e = gsr::launch_pair(tmA, tmB, tmC, p, clusters, stream);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }
 
@@ -279,8 +315,9 @@ gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int
         return e == cudaSuccess ? GSR_OK : cuda_fail(e);
     }
     if ((s = load_encoder()) != GSR_OK) return s;
-    if (choose_path(M) == 1)
-        return run_skinny(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
+    const int path = choose_path(M, N, info.num_sms);
+    if (path == 1) return run_skinny(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
+    if (path == 2) return run_pair(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
     return run_tiled(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
 }
 
@@ -384,9 +421,17 @@ gsr_status gsr_device_status(CUstream_st* stream, int* code) {
 }
 
 int gsr_select_path(int64_t M, int64_t N, int64_t K) {
-    (void)N;
     (void)K;
-    return choose_path(M);
+    int sms = kDefaultSms;
+    int dev = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+            auto it = g_devices.find(dev);
+            if (it != g_devices.end()) sms = it->second.num_sms;
+        }
+    }
+    return choose_path(M, N, sms);
 }
 
 void gsr_set_path_override(int path) { g_path_override.store(path, std::memory_order_relaxed); }

@@ -56,6 +56,13 @@ struct SkinnyParams {
 cudaError_t launch_tiled(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                          const TiledParams& p, int bn, int grid, cudaStream_t stream);
 
+// Paired tiled path: clusters of 2 CTAs, 256 x 256 tiles, cta_group::2 MMA.
+// grid = 2 * clusters, clusters <= pair_max_active_clusters().
+cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const TiledParams& p, int clusters, cudaStream_t stream);
+int pair_max_active_clusters();
+int pair_smem_bytes();
+
 // Skinny path (M <= 64): C^T = B^T A^T on 128-row tiles of N, stream-K split of K.
 // mp is the MMA N (16, 32 or 64).
 cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,

@@ -94,10 +94,14 @@ def test_path_selection_and_override():
     try:
         assert gsr.select_path(16, 16384, 16384) == 1
         assert gsr.select_path(64, 8, 8) == 1
-        assert gsr.select_path(65, 8, 8) == 0
-        assert gsr.select_path(8192, 8192, 8192) == 0
+        assert gsr.select_path(65, 8, 8) == gsr.KERNEL_TILED
+        assert gsr.select_path(8192, 8192, 8192) == gsr.KERNEL_PAIR
+        assert gsr.select_path(1024, 1024, 1024) == gsr.KERNEL_TILED
         gsr.set_path_override(gsr.PATH_TILED)
         assert gsr.select_path(16, 16384, 16384) == 0
+        assert gsr.select_path(8192, 8192, 8192) == 0
+        gsr.set_path_override(gsr.PATH_PAIR)
+        assert gsr.select_path(1024, 1024, 1024) == gsr.KERNEL_PAIR
         gsr.set_path_override(gsr.PATH_SKINNY)
         assert gsr.select_path(16, 8, 8) == 1
         assert gsr.select_path(100, 8, 8) == 0      # small-M path needs M <= 64

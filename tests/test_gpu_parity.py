@@ -118,8 +118,8 @@ def test_edges_auto(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (129, 264, 72), (255, 120, 200), (257, 392, 136),
                                    (16, 16384, 1024), (640, 768, 4096)])
-@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128])
-def test_edges_both_tile_widths(M, N, K, path):
+@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_PAIR])
+def test_edges_every_tiled_kernel(M, N, K, path):
     parity(M, N, K, 1.0, path=path, seed=7 * M + N + K)
 
 
@@ -132,6 +132,19 @@ def test_small_m_path(M, N, K):
     parity(M, N, K, 0.75, path=gsr.PATH_SKINNY, seed=M * N + K, b_scaled=True)
 
 
+@pytest.mark.parametrize("name", ["square1024", "ragged2000x3000x1000"])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_PAIR])
+def test_small_workloads_on_each_tiled_kernel(name, path):
+    w = WORKLOADS[name]
+    parity(w.M, w.N, w.K, w.alpha, path=path)
+
+
+def test_big_workloads_use_the_pair_kernel():
+    for name in ("square8192", "llm_mlp_up"):
+        w = WORKLOADS[name]
+        assert gsr.select_path(w.M, w.N, w.K) == gsr.KERNEL_PAIR
+
+
 def test_skinny_workload_through_tiled_path():
     w = WORKLOADS["skinny_decode"]
     parity(w.M, w.N, w.K, w.alpha, path=gsr.PATH_TILED, b_scaled=True)
@@ -140,7 +153,8 @@ def test_skinny_workload_through_tiled_path():
 # ---------------------------------------------------------------------------- structure
 
 @pytest.mark.parametrize("M,K,path", [(64, 64, gsr.PATH_AUTO), (130, 72, gsr.PATH_AUTO),
-                                      (300, 256, gsr.PATH_TILED_128), (40, 136, gsr.PATH_SKINNY)])
+                                      (300, 256, gsr.PATH_TILED_128), (40, 136, gsr.PATH_SKINNY),
+                                      (520, 264, gsr.PATH_PAIR)])
 def test_identity_b_is_exact(M, K, path):
     # the sum has one non-zero term, so fp32 accumulation is exact and C must equal the
     # oracle bit for bit
@@ -153,7 +167,8 @@ def test_identity_b_is_exact(M, K, path):
 
 @pytest.mark.parametrize("M,N,K,alpha,path", [(200, 264, 1000, 0.5, gsr.PATH_AUTO),
                                               (8, 64, 3000, 1.0, gsr.PATH_SKINNY),
-                                              (130, 128, 2048, 1.0, gsr.PATH_TILED_256)])
+                                              (130, 128, 2048, 1.0, gsr.PATH_TILED_256),
+                                              (300, 520, 1000, 0.5, gsr.PATH_PAIR)])
 def test_all_ones_is_exact(M, N, K, alpha, path):
     A = torch.ones(M, K, dtype=torch.float16)
     B = torch.ones(K, N, dtype=torch.float16)
@@ -161,7 +176,7 @@ def test_all_ones_is_exact(M, N, K, alpha, path):
     assert torch.all(C == float(np.float16(alpha * K)))
 
 
-@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_SKINNY])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_SKINNY, gsr.PATH_PAIR])
 def test_one_hot_rows(path):
     M, N, K = 48, 392, 320
     rng = np.random.default_rng(4)
