@@ -156,7 +156,8 @@ void gsr_set_wait_timeout_ns(uint64_t ns);
 
 /* Test-only switches, 0 in normal use.  Bit 0: the first CTA's producer skips
  * its first shared-memory fill, so that CTA's waits run out (exercises the
- * bounded-wait path without faulting the GPU). */
+ * bounded-wait path without faulting the GPU).  Bit 1: the tiled kernels copy B
+ * as separate 64-column boxes even where one 3-D copy per stage would do. */
 void gsr_set_test_flags(uint32_t flags);
 
 /* CUDA error code of the last failing CUDA call on this host thread (0: none). */

@@ -113,23 +113,26 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (both CTAs)
-        const uint64_t pol = l2_policy_evict_last();
-        uint32_t stage = 0, phase = 0;
-        uint32_t armed_mask = 0, armed_parity = 0;
-        bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
-        bool ok = true;
-        for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
-            int mb, nb;
-            pair_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
-            const int m_row = mb * Cfg::BM + (int)rank * Cfg::HALF_M;
-            const int n_col = nb * Cfg::BN + (int)rank * Cfg::HALF_N;
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                bool got = true;
-                if (lane == 0) got = w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty);
-                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-                if (lane == 0) {
+        // One thread issues every copy: per stage, this CTA's 128 A rows and its 128 B
+        // columns (one 3-D box when B is described as 64-column chunks, else two 2-D boxes).
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed_mask = 0, armed_parity = 0;
+            bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
+                int mb, nb;
+                pair_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+                const int m_row = mb * Cfg::BM + (int)rank * Cfg::HALF_M;
+                const int n_col = nb * Cfg::BN + (int)rank * Cfg::HALF_N;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
                     if (drop_first) {
-                        drop_first = false;
+                        drop_first = false;   // test hook: this stage is never filled
                     } else {
                         const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
                         if (rank == 0) {
@@ -139,18 +142,19 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
                         }
                         tma_load_2d_pair(sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES, &tmA,
                                          leader_full, kb * Cfg::BK, m_row, pol);
+                        const uint32_t b_dst = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
+                        if (p.b_chunked) {
+                            tma_load_3d_pair(b_dst, &tmB, leader_full, 0, kb * Cfg::BK, n_col / 64, pol);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < Cfg::HALF_N / 64; ++j)
-                            tma_load_2d_pair(sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES +
-                                                 j * Cfg::B_CHUNK_BYTES,
-                                             &tmB, leader_full, n_col + j * 64, kb * Cfg::BK, pol);
+                            for (int j = 0; j < Cfg::HALF_N / 64; ++j)
+                                tma_load_2d_pair(b_dst + j * Cfg::B_CHUNK_BYTES, &tmB, leader_full,
+                                                 n_col + j * 64, kb * Cfg::BK, pol);
+                        }
                     }
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
-                __syncwarp();
-                if (++stage == S) { stage = 0; phase ^= 1u; }
             }
-        }
-        if (lane == 0) {
             // Leader: every stage it armed completes only once both CTAs' bytes landed.
             for (int s = 0; s < S; ++s)
                 if (armed_mask & (1u << s)) w.drain(full_bar(s), (armed_parity >> s) & 1u);
@@ -166,44 +170,37 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader)
-        if (rank == 0) {
+        // One thread, no warp-wide synchronisation per k-block: the tensor pipe must never
+        // wait on the issuing loop.
+        if (rank == 0 && lane == 0) {
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true;
             for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters, ++it) {
                 const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
-                bool got = true;
-                if (lane == 0) got = w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty);
-                if (!__shfl_sync(0xffffffffu, got, 0)) break;
+                if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
                 tcgen05_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::BN;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if (lane == 0) got = w.wait(full_bar(stage), phase, kDevErrMmaFull);
-                    if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                    if (!w.wait(full_bar(stage), phase, kDevErrMmaFull)) { ok = false; break; }
                     tcgen05_fence_after();
-                    if (lane == 0) {
-                        const uint32_t a0 = sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES;
-                        const uint32_t b0 = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
+                    const uint32_t a0 = sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES;
+                    const uint32_t b0 = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
 #pragma unroll
-                        for (int k = 0; k < Cfg::BK / 16; ++k) {
-                            const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(b0 + k * 2048, Cfg::B_CHUNK_BYTES, 1024);
-                            mma_f16_ss_pair(d_tmem, ad, bd, Cfg::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
-                        }
-                        mma_commit_pair(empty_bar(stage), 0x3);   // frees the stage in both CTAs
+                    for (int k = 0; k < Cfg::BK / 16; ++k) {
+                        const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(b0 + k * 2048, Cfg::B_CHUNK_BYTES, 1024);
+                        mma_f16_ss_pair(d_tmem, ad, bd, Cfg::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    __syncwarp();
+                    mma_commit_pair(empty_bar(stage), 0x3);
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if (lane == 0) mma_commit_pair(tfull_bar(acc), 0x3);   // both halves of D ready
-                __syncwarp();
+                mma_commit_pair(tfull_bar(acc), 0x3);
             }
-            if (lane == 0) {
-                mma_commit_pair(drain_bar, 0x1);
-                w.drain(drain_bar, 0);
-            }
-            __syncwarp();
+            mma_commit_pair(drain_bar, 0x1);
+            w.drain(drain_bar, 0);
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quad = warp & 3;

@@ -86,6 +86,27 @@ gsr_status encode_fp16_2d(CUtensorMap* map, const void* base, uint64_t rows, uin
     return GSR_OK;
 }
 
+// Row-major fp16 B (K x N, N % 64 == 0) seen as 64-column chunks: a 3-D tensor map
+// {64 columns, K rows, N/64 chunks} whose box {64, box_k, box_chunks} lands box_chunks
+// consecutive chunks one after the other in shared memory, each box_k rows of 128 bytes
+// (the same layout as box_chunks separate 64 x box_k boxes), in one copy instruction.
+gsr_status encode_fp16_chunked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                               uint32_t box_rows, uint32_t box_chunks) {
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return GSR_ERR_CUDA;
+    }
+    return GSR_OK;
+}
+
 // Checks that need no GPU: sizes, null pointers, alignment, aliasing.  `*nothing` is set
 // when there is no output to produce.
 gsr_status validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
@@ -225,6 +246,7 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
     p.num_k_blocks = kb;
     p.num_tiles = mb * nb;
     p.group_m = kGroupM;
+    p.b_chunked = 0;
     p.err = st.err;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
@@ -239,10 +261,17 @@ gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, 
     gsr_status s = stream_state(dev, stream, 0, 0, &st);
     if (s != GSR_OK) return s;
     CUtensorMap tmA, tmB, tmC;
+    const bool chunked = (N % 64) == 0 &&
+                         !(g_test_flags.load(std::memory_order_relaxed) & gsr::kTestNoChunkedB);
     if ((s = encode_fp16_2d(&tmA, A, M, K, 64, 128)) != GSR_OK) return s;
-    if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) return s;
+    if (chunked) {
+        if ((s = encode_fp16_chunked(&tmB, B, K, N, 64, 2)) != GSR_OK) return s;
+    } else if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) {
+        return s;
+    }
     if ((s = encode_fp16_2d(&tmC, C, M, N, 64, 128)) != GSR_OK) return s;
     gsr::TiledParams p;
+    p.b_chunked = chunked ? 1 : 0;
     p.M = M;
     p.N = N;
     p.K = K;

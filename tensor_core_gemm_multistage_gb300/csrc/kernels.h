@@ -25,6 +25,7 @@ enum DeviceError : int {
 // Test-only flags (gsr_set_test_flags).
 enum TestFlags : uint32_t {
     kTestDropFirstLoad = 1u,    // CTA 0's producer skips its first stage fill
+    kTestNoChunkedB = 2u,       // host: copy B as separate 64-column boxes even when N % 64 == 0
 };
 
 struct TiledParams {
@@ -34,6 +35,7 @@ struct TiledParams {
     int* err;               // device error word
     uint64_t timeout_ns;    // bound on every mbarrier wait
     uint32_t test_flags;
+    int b_chunked;          // tmB is the 3-D view {64, K, N/64} of B (N % 64 == 0)
 };
 
 struct SkinnyParams {

@@ -139,6 +139,21 @@ def test_small_workloads_on_each_tiled_kernel(name, path):
     parity(w.M, w.N, w.K, w.alpha, path=path)
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 1024, 1024), (300, 768, 200)])
+def test_pair_kernel_with_and_without_3d_b_copies(M, N, K):
+    # N % 64 == 0: B normally arrives as one 3-D copy per stage; test flag bit 1 forces the
+    # two-box 2-D copies.  Both must match the oracle.
+    A, B = make_inputs(M, N, K, seed=M + N + K)
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, return_pre=True)
+    for flags in (0, 2):
+        gsr.set_test_flags(flags)
+        try:
+            C = run_gpu(A, B, 0.5, gsr.PATH_PAIR)
+        finally:
+            gsr.set_test_flags(0)
+        check(C, ref, z, "pair flags=%d" % flags)
+
+
 def test_big_workloads_use_the_pair_kernel():
     for name in ("square8192", "llm_mlp_up"):
         w = WORKLOADS[name]
