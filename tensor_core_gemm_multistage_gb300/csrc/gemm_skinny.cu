@@ -114,22 +114,24 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        const uint64_t pol_stream = l2_policy_evict_first();   // B: every byte read once
-        const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every CTA
-        uint32_t stage = 0, phase = 0;
-        uint32_t armed_mask = 0, armed_parity = 0;
-        bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
-        bool ok = true;
-        for (long long pos = my_begin; ok && pos < my_end;) {
-            const int tile = (int)(pos / kbpt);
-            const int kb0 = (int)(pos % kbpt);
-            const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
-            const int n0 = tile * Cfg::TN;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                bool got = true;
-                if (lane == 0) got = w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty);
-                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-                if (lane == 0) {
+        // One lane issues everything, with no warp-wide synchronisation per stage.
+        if (lane == 0) {
+            const uint64_t pol_stream = l2_policy_evict_first();   // B: every byte read once
+            const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every CTA
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed_mask = 0, armed_parity = 0;
+            bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+            bool ok = true;
+            for (long long pos = my_begin; ok && pos < my_end;) {
+                const int tile = (int)(pos / kbpt);
+                const int kb0 = (int)(pos % kbpt);
+                const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+                const int n0 = tile * Cfg::TN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
                     if (drop_first) {
                         drop_first = false;
                     } else {
@@ -144,34 +146,32 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         armed_mask |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
-                __syncwarp();
-                if (++stage == S) { stage = 0; phase ^= 1u; }
+                pos += kb1 - kb0;
             }
-            pos += kb1 - kb0;
-        }
-        if (lane == 0)
             for (int s = 0; s < S; ++s)
                 if (armed_mask & (1u << s)) w.drain(full_bar(s), (armed_parity >> s) & 1u);
+        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        uint32_t stage = 0, phase = 0, it = 0;
-        bool ok = true;
-        for (long long pos = my_begin; ok && pos < my_end; ++it) {
-            const int kb0 = (int)(pos % kbpt);
-            const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
-            const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
-            bool got = true;
-            if (lane == 0) got = w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty);
-            if (!__shfl_sync(0xffffffffu, got, 0)) break;
-            tcgen05_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * MP;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (lane == 0) got = w.wait(full_bar(stage), phase, kDevErrMmaFull);
-                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, it = 0;
+            bool ok = true;
+            for (long long pos = my_begin; ok && pos < my_end; ++it) {
+                const int kb0 = (int)(pos % kbpt);
+                const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+                const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
+                if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
                 tcgen05_fence_after();
-                if (lane == 0) {
+                const uint32_t d_tmem = tmem_base + acc * MP;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!w.wait(full_bar(stage), phase, kDevErrMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after();
                     const uint32_t bt = sb + Cfg::OFF_BT + stage * Cfg::BT_STAGE_BYTES;
                     const uint32_t at = sb + Cfg::OFF_AT + stage * Cfg::AT_STAGE_BYTES;
 #pragma unroll
@@ -183,16 +183,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         mma_f16_ss(d_tmem, ad, bd, Cfg::IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
-                __syncwarp();
-                if (++stage == S) { stage = 0; phase ^= 1u; }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));
+                pos += kb1 - kb0;
             }
-            if (!ok) break;
-            if (lane == 0) mma_commit(tfull_bar(acc));
-            __syncwarp();
-            pos += kb1 - kb0;
-        }
-        if (lane == 0) {
             mma_commit(drain_bar);
             w.drain(drain_bar, 0);
         }

@@ -118,18 +118,20 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        uint32_t stage = 0, phase = 0;
-        uint32_t armed_mask = 0, armed_parity = 0;   // last phase each stage was filled in
-        bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            int mb, nb;
-            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                bool got = true;
-                if (lane == 0) got = w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty);
-                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-                if (lane == 0) {
+        // One lane issues everything, with no warp-wide synchronisation per stage.
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed_mask = 0, armed_parity = 0;   // last phase each stage was filled in
+            bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
                     if (drop_first) {
                         drop_first = false;   // test hook: this stage is never filled
                     } else {
@@ -144,32 +146,31 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         armed_mask |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
-                __syncwarp();
-                if (++stage == S) { stage = 0; phase ^= 1u; }
             }
-        }
-        // Every copy this CTA started must land before the CTA may exit.
-        if (lane == 0)
+            // Every copy this CTA started must land before the CTA may exit.
             for (int s = 0; s < S; ++s)
                 if (armed_mask & (1u << s)) w.drain(full_bar(s), (armed_parity >> s) & 1u);
+        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        uint32_t stage = 0, phase = 0, it = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
-            const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
-            bool got = true;
-            if (lane == 0) got = w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty);
-            if (!__shfl_sync(0xffffffffu, got, 0)) break;
-            tcgen05_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * Cfg::BN;
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                if (lane == 0) got = w.wait(full_bar(stage), phase, kDevErrMmaFull);
-                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        // One lane issues every MMA and commit; the tensor pipe must never wait on the loop.
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+                const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
+                if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
                 tcgen05_fence_after();
-                if (lane == 0) {
+                const uint32_t d_tmem = tmem_base + acc * Cfg::BN;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!w.wait(full_bar(stage), phase, kDevErrMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after();
                     const uint32_t a0 = sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES;
                     const uint32_t b0 = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
 #pragma unroll
@@ -181,16 +182,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         mma_f16_ss(d_tmem, ad, bd, Cfg::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
-                __syncwarp();
-                if (++stage == S) { stage = 0; phase ^= 1u; }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));   // accumulator ready for the epilogue
             }
-            if (!ok) break;
-            if (lane == 0) mma_commit(tfull_bar(acc));   // accumulator ready for the epilogue
-            __syncwarp();
-        }
-        // Every MMA this thread issued must finish before tensor memory is released.
-        if (lane == 0) {
+            // Every MMA this thread issued must finish before tensor memory is released.
             mma_commit(drain_bar);
             w.drain(drain_bar, 0);
         }
