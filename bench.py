@@ -345,6 +345,26 @@ def run_gsr(args, w):
     if sampler is not None:
         sampler.stop()
 
+    # Context only (the tutorial compares its fused kernel with unfused PyTorch): the same
+    # workload as torch.relu((A @ B) * alpha) and as a plain cuBLAS fp16 matmul.
+    context = None
+    if args.torch_context:
+        context = {}
+        for label, fn in (("torch_unfused_relu_matmul_scale", lambda: torch.relu((dA @ dB) * w.alpha)),
+                          ("cublas_matmul_only", lambda: torch.matmul(dA, dB, out=dC))):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            c1.record(stream)
+            torch.cuda.synchronize()
+            ms = c0.elapsed_time(c1) / args.steps
+            context[label] = {"ms_per_step": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12}
+
     if rank != 0:
         return 0
 
@@ -377,6 +397,8 @@ def run_gsr(args, w):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if context is not None:
+        line["context"] = context
     if sampler is not None:
         line["clocks"] = sampler.summary(t_wall0, t_wall1)
     if world == 1 and args.cpu_seconds > 0:
@@ -400,6 +422,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--torch-context", action="store_true",
+                    help="also time torch.relu((A@B)*alpha) and a plain cuBLAS matmul (context)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
