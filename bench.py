@@ -252,8 +252,9 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w):
+def config_of(w, epilogue="scale_relu"):
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+            "epilogue": epilogue,
             "inputs": "A,B fp16 from seeded randn" + (", B*K^-1/2" if w.b_std_inv_sqrt_k else ""),
             "accumulate": "f32", "output": "f16",
             "l2": ("inputs larger than L2 (A+B %d MiB > 126 MiB), no flush"
@@ -285,8 +286,18 @@ def run_gsr(args, w):
     path = gsr.select_path(w.M, w.N, w.K)
     kernel = KERNEL_NAMES[path]
 
-    def step():
-        gsr.gemm_scale_relu(dA, dB, dC, w.alpha, stream=stream)
+    if args.epilogue == "bias_gelu":
+        from tensor_core_gemm_multistage_gb300.workloads import make_bias
+        dbias = make_bias(w.N, seed=1).to(dev)
+
+        def step():
+            gsr.gemm_bias_gelu(dA, dB, dbias, dC, stream=stream)
+    elif args.epilogue == "scale":
+        def step():
+            gsr.gemm_scale(dA, dB, dC, w.alpha, stream=stream)
+    else:
+        def step():
+            gsr.gemm_scale_relu(dA, dB, dC, w.alpha, stream=stream)
 
     sampler = ClockSampler(gpu_uuid()).start() if rank == 0 else None
     for _ in range(args.warmup):
@@ -325,7 +336,7 @@ def run_gsr(args, w):
 
     # end-to-end through the host entry point: pinned host in, pinned host out
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and args.epilogue == "scale_relu":
         hA, hB = A.pin_memory(), B.pin_memory()
         hC = torch.empty(w.M, w.N, dtype=torch.float16).pin_memory()
         gsr.gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, w.alpha, stream=stream)
@@ -390,7 +401,7 @@ def run_gsr(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic (seeded randn, fp16)", "config": config_of(w),
+        "data": "synthetic (seeded randn, fp16)", "config": config_of(w, args.epilogue),
         "roofline": roofline,
         "kernel_ms": kernel_avg_ms,
         "gpu_launches": args.steps,
@@ -422,6 +433,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--epilogue", choices=["scale_relu", "scale", "bias_gelu"], default="scale_relu",
+                    help="scale_relu: the fused operator (default); scale: alpha*A@B; "
+                         "bias_gelu: GELU(A@B + bias)")
     ap.add_argument("--torch-context", action="store_true",
                     help="also time torch.relu((A@B)*alpha) and a plain cuBLAS matmul (context)")
     args = ap.parse_args(argv)

@@ -82,6 +82,31 @@ gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int
                            int64_t K, float alpha, struct CUstream_st* stream);
 
 /*
+ * C = alpha * A.B, the same GEMM without the ReLU; alpha = 1 gives the plain
+ * tiled matrix product.  ("TileLang: создание высокопроизводительных GPU-ядер"
+ * survey page, section 2 "Тилированное умножение матриц": make_matmul, the plain
+ * tiled tensor-core GEMM the fused operator extends.)  Arguments, layout,
+ * ownership, paths and errors as for gemm_scale_relu; K == 0 gives zeros.
+ */
+gsr_status gemm_scale(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                      float alpha, struct CUstream_st* stream);
+
+/*
+ * C[m,n] = GELU( sum_k A[m,k] * B[k,n] + bias[n] ), GELU in its tanh form
+ * 0.5 x (1 + tanh( sqrt(2/pi) (x + 0.044715 x^3) )), computed in fp32 on the
+ * accumulator before the fp16 store.  (Same survey page, section 4 "Слияние
+ * эпиколов: GEMM + Bias + GELU": make_matmul_bias_gelu adds the bias and applies
+ * an exponential-formula GELU approximation in registers.)
+ *
+ *   bias   device pointer to N float16 values, 16-byte aligned, must not
+ *          overlap C; read, never written.
+ * Other arguments, paths and errors as for gemm_scale_relu.  K == 0 gives
+ * C[m,n] = GELU(bias[n]).
+ */
+gsr_status gemm_bias_gelu(const void* A, const void* B, const void* bias, void* C, int64_t M,
+                          int64_t N, int64_t K, struct CUstream_st* stream);
+
+/*
  * gemm_scale_relu with the operands in host memory: copies A and B host ->
  * device into the caller's device buffers dA and dB, runs gemm_scale_relu
  * into dC and copies C back device -> host, all queued on `stream`.  The host

@@ -9,6 +9,9 @@ The arithmetic lives in ``gsr_oracle.c`` (plain C, built with gcc); this module
 only builds that file and marshals numpy arrays through ctypes.
 
 Sources (page title and section):
+  * the aikraft.ru TileLang tutorial survey ("TileLang: создание высокопроизводительных
+    GPU-ядер"), sections 2 (make_matmul, plain tiled GEMM) and 4 (make_matmul_bias_gelu) for
+    the further epilogues of ``gemm_epilogue``;
   * "Tutorial14: 使用TileLang语言编写attention算子", section 3 (operator formula)
     and section 2 (the gemm_fused kernel: fp16 inputs, float accumulator,
     multiply by the float32 scale, then max with 0, fp16 output);
@@ -64,6 +67,10 @@ def _load():
         lib.oracle_gemm_scale_relu.argtypes = [
             u16p, u16p, u16p, f64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_float, i64p, ctypes.c_int64]
+        lib.oracle_gemm_epilogue.restype = ctypes.c_int
+        lib.oracle_gemm_epilogue.argtypes = [
+            u16p, u16p, u16p, u16p, f64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_float, ctypes.c_int, i64p, ctypes.c_int64]
         lib.oracle_f16_decode_array.restype = None
         lib.oracle_f16_decode_array.argtypes = [u16p, f64p, ctypes.c_int64]
         lib.oracle_f16_encode_array.restype = None
@@ -135,6 +142,55 @@ def gemm_scale_relu(A, B, alpha: float, rows=None, return_pre: bool = False):
         raise MemoryError("oracle ran out of memory")
     c16 = c.view(np.float16)
     return (c16, z) if return_pre else c16
+
+
+EPI_SCALE_RELU, EPI_SCALE, EPI_BIAS_GELU = 0, 1, 2
+
+
+def gemm_epilogue(A, B, alpha: float = 1.0, kind: int = EPI_SCALE_RELU, bias=None, rows=None,
+                  return_pre: bool = False):
+    """C = epilogue(A @ B) for fp16 A (M,K), B (K,N), summed in fp64.
+
+    kind 0: ReLU(alpha * sum); 1: alpha * sum; 2: GELU(sum + bias) (tanh form written with
+    the exponential as x / (1 + exp(-2u)); ``bias`` fp16 of length N).  With ``return_pre`` also returns Y, the fp64
+    value before the final rounding to fp16.
+    """
+    lib = _load()
+    a = _as_bits(A)
+    b = _as_bits(B)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError("shape mismatch: A %s, B %s" % (a.shape, b.shape))
+    M, K = a.shape
+    N = b.shape[1]
+    if kind == EPI_BIAS_GELU:
+        bb = _as_bits(bias).reshape(-1)
+        if bb.shape[0] != N:
+            raise ValueError("bias must have N = %d values" % N)
+    else:
+        bb = np.zeros(max(N, 1), np.uint16)
+    if rows is None:
+        R, rows_arr = M, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        R = rows_arr.shape[0]
+    c = np.zeros((R, N), dtype=np.uint16)
+    y = np.zeros((R, N), dtype=np.float64) if return_pre else None
+    a_buf = a if a.size else np.zeros(1, np.uint16)
+    b_buf = b if b.size else np.zeros(1, np.uint16)
+    bb_buf = bb if bb.size else np.zeros(1, np.uint16)
+    c_buf = c if c.size else np.zeros(1, np.uint16)
+    rc = lib.oracle_gemm_epilogue(
+        _ptr(a_buf, ctypes.c_uint16), _ptr(b_buf, ctypes.c_uint16), _ptr(bb_buf, ctypes.c_uint16),
+        _ptr(c_buf, ctypes.c_uint16),
+        _ptr(y, ctypes.c_double) if (y is not None and y.size) else None,
+        M, N, K, ctypes.c_float(alpha), int(kind),
+        _ptr(rows_arr, ctypes.c_int64) if rows_arr is not None and R else None, R)
+    if rc == -1:
+        raise ValueError("oracle rejected the arguments")
+    if rc != 0:
+        raise MemoryError("oracle ran out of memory")
+    c16 = c.view(np.float16)
+    return (c16, y) if return_pre else c16
 
 
 def f16_decode(bits) -> np.ndarray:

@@ -39,6 +39,7 @@
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -fopenmp
  * (no fast-math; the default round-to-nearest mode is assumed by rint()).
  */
+#define _DEFAULT_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -179,6 +180,85 @@ int oracle_gemm_scale_relu(const uint16_t *A, const uint16_t *B, uint16_t *C,
             double y = z > 0.0 ? z : 0.0;          /* ... then ReLU    */
             if (Z)
                 Z[r * N + n] = z;
+            C[r * N + n] = oracle_f16_encode(y);
+        }
+        free(acc);
+    }
+    return failed ? -2 : 0;
+}
+
+/* ---- further epilogues on the same sum -------------------------------------
+ *
+ * kind 0: ReLU(alpha * sum)               (same result as oracle_gemm_scale_relu)
+ * kind 1: alpha * sum                      (the plain tiled GEMM when alpha == 1: the
+ *                                           make_matmul section of the aikraft.ru TileLang
+ *                                           tutorial survey, "Тилированное умножение матриц")
+ * kind 2: GELU(sum + bias[n])              (its make_matmul_bias_gelu section, "Слияние
+ *                                           эпиколов: GEMM + Bias + GELU": bias added, then
+ *                                           a GELU approximation written with an exponential)
+ *
+ * GELU reading: the tanh approximation 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))),
+ * written through the exponential as x / (1 + exp(-2u)) with u = sqrt(2/pi)(x + 0.044715 x^3)
+ * (the same function, since 1 + tanh(u) = 2 / (1 + exp(-2u)); this form has no cancellation
+ * for large negative x).  bias holds N
+ * binary16 values (ignored unless kind == 2).  Y (optional) receives the fp64 value that
+ * is rounded into C.  Rows as for oracle_gemm_scale_relu.  Returns 0, -1 (bad argument)
+ * or -2 (out of memory). */
+static double gelu_exp_form(double x)
+{
+    const double u = sqrt(2.0 / M_PI) * (x + 0.044715 * x * x * x);
+    return x / (1.0 + exp(-2.0 * u));
+}
+
+int oracle_gemm_epilogue(const uint16_t *A, const uint16_t *B, const uint16_t *bias,
+                         uint16_t *C, double *Y, int64_t M, int64_t N, int64_t K,
+                         float alpha, int kind, const int64_t *rows, int64_t nrows)
+{
+    if (M < 0 || N < 0 || K < 0 || kind < 0 || kind > 2)
+        return -1;
+    int64_t R = rows ? nrows : M;
+    if (R < 0)
+        return -1;
+    if (rows)
+        for (int64_t r = 0; r < R; ++r)
+            if (rows[r] < 0 || rows[r] >= M)
+                return -1;
+    if (R == 0 || N == 0)
+        return 0;
+    if (!C || (K > 0 && (!A || !B)) || (kind == 2 && !bias))
+        return -1;
+    build_decode_table();
+
+    const double alpha_d = (double)alpha;
+    int failed = 0;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        double *acc = (double *)calloc((size_t)N, sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        for (int64_t k = 0; k < K; ++k) {
+            double a = g_dec[A[i * K + k]];
+            const uint16_t *brow = B + k * N;
+            for (int64_t n = 0; n < N; ++n)
+                acc[n] += a * g_dec[brow[n]];
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            double y;
+            if (kind == 0) {
+                double z = alpha_d * acc[n];
+                y = z > 0.0 ? z : 0.0;
+            } else if (kind == 1) {
+                y = alpha_d * acc[n];
+            } else {
+                y = gelu_exp_form(acc[n] + g_dec[bias[n]]);
+            }
+            if (Y)
+                Y[r * N + n] = y;
             C[r * N + n] = oracle_f16_encode(y);
         }
         free(acc);

@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
                                        ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int)
         L.gemm_scale_relu.restype = i32
         L.gemm_scale_relu.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
+        L.gemm_scale.restype = i32
+        L.gemm_scale.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
+        L.gemm_bias_gelu.restype = i32
+        L.gemm_bias_gelu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.gemm_scale_relu_noalloc.restype = i32
         L.gemm_scale_relu_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
         L.gemm_scale_relu_host.restype = i32
@@ -186,6 +190,54 @@ def gemm_scale_relu(A, B, C, alpha: float, stream=None):
     if s != Status.OK:
         raise GsrError(s, "gemm_scale_relu")
     return C
+
+
+def _operands(A, B, C):
+    _check_matrix(A, "A")
+    M, K = A.shape
+    _check_matrix(B, "B")
+    if B.shape[0] != K:
+        raise ValueError("inner sizes differ: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    N = B.shape[1]
+    _check_matrix(C, "C", (M, N))
+    dev = C.device
+    if dev.type != "cuda" or A.device != dev or B.device != dev:
+        raise ValueError("A, B and C must be CUDA tensors on one device")
+    return M, N, K, dev
+
+
+def gemm_scale(A, B, C, alpha: float = 1.0, stream=None):
+    """C = alpha * A @ B into the preallocated fp16 tensor C (alpha = 1: plain GEMM)."""
+    import torch
+    M, N, K, dev = _operands(A, B, C)
+    with torch.cuda.device(dev):
+        s = lib().gemm_scale(A.data_ptr() or None, B.data_ptr() or None, C.data_ptr() or None,
+                             M, N, K, ctypes.c_float(alpha), _stream_handle(stream, dev) or None)
+    if s != Status.OK:
+        raise GsrError(s, "gemm_scale")
+    return C
+
+
+def gemm_bias_gelu(A, B, bias, C, stream=None):
+    """C = GELU(A @ B + bias) (tanh form), bias an fp16 CUDA vector of length N."""
+    import torch
+    M, N, K, dev = _operands(A, B, C)
+    if not isinstance(bias, torch.Tensor) or bias.dtype != torch.float16 or bias.dim() != 1 \
+            or bias.shape[0] != N or not bias.is_contiguous() or bias.device != dev:
+        raise ValueError("bias must be a contiguous float16 CUDA vector of length N on C's device")
+    with torch.cuda.device(dev):
+        s = lib().gemm_bias_gelu(A.data_ptr() or None, B.data_ptr() or None,
+                                 bias.data_ptr() or None, C.data_ptr() or None, M, N, K,
+                                 _stream_handle(stream, dev) or None)
+    if s != Status.OK:
+        raise GsrError(s, "gemm_bias_gelu")
+    return C
+
+
+def gemm_bias_gelu_ptr(A: int, B: int, bias: int, C: int, M: int, N: int, K: int,
+                       stream: int = 0) -> int:
+    return lib().gemm_bias_gelu(A or None, B or None, bias or None, C or None, M, N, K,
+                                stream or None)
 
 
 def gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, alpha: float, stream=None):

@@ -51,4 +51,58 @@ struct Waiter {
     __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
 };
 
+// ---------------------------------------------------------------------------
+// Epilogue functions on the fp32 accumulator
+// ---------------------------------------------------------------------------
+// GELU, tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + tanhf(u));
+}
+
+__device__ __forceinline__ float epilogue_value(float acc, float alpha, float bias, int epi) {
+    if (epi == kEpiScaleRelu) return fmaxf(acc * alpha, 0.0f);
+    if (epi == kEpiScale) return acc * alpha;
+    return gelu_tanh(acc + bias);
+}
+
+// Eight consecutive accumulator columns (fp32 bit patterns) -> eight fp16 in a uint4.
+// `col0` is the first column's index in C (a multiple of 8); its bias values are read
+// only when the columns lie inside C (N is a multiple of 8, so all eight or none do).
+__device__ __forceinline__ uint4 epilogue_8(const uint32_t* src, float alpha, int epi,
+                                            const __half* bias, int col0, int N) {
+    uint4 v;
+    if (epi == kEpiScaleRelu) {
+        v.x = scale_relu_pack(src[0], src[1], alpha);
+        v.y = scale_relu_pack(src[2], src[3], alpha);
+        v.z = scale_relu_pack(src[4], src[5], alpha);
+        v.w = scale_relu_pack(src[6], src[7], alpha);
+        return v;
+    }
+    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (epi == kEpiBiasGelu && col0 < N) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(bias + col0));
+        const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(h[i]);
+            b[2 * i] = f.x;
+            b[2 * i + 1] = f.y;
+        }
+    }
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = epilogue_value(__uint_as_float(src[2 * i]), alpha, b[2 * i], epi);
+        const float hi = epilogue_value(__uint_as_float(src[2 * i + 1]), alpha, b[2 * i + 1], epi);
+        __half2 h2 = __floats2half2_rn(lo, hi);
+        out[i] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    v.x = out[0];
+    v.y = out[1];
+    v.z = out[2];
+    v.w = out[3];
+    return v;
+}
+
 }  // namespace gsr

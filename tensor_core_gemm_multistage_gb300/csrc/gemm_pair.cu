@@ -243,11 +243,7 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t* src = (j < 4) ? (r0 + 8 * j) : (r1 + 8 * (j - 4));
-                    uint4 v;
-                    v.x = scale_relu_pack(src[0], src[1], p.alpha);
-                    v.y = scale_relu_pack(src[2], src[3], p.alpha);
-                    v.z = scale_relu_pack(src[4], src[5], p.alpha);
-                    v.w = scale_relu_pack(src[6], src[7], p.alpha);
+                    const uint4 v = epilogue_8(src, p.alpha, p.epi, p.bias, n0 + c * 64 + 8 * j, p.N);
                     *reinterpret_cast<uint4*>(crow + ((j ^ (row & 7)) << 4)) = v;
                 }
                 fence_proxy_async_smem();

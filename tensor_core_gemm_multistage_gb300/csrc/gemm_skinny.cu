@@ -266,10 +266,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
             }
             if (store && n < p.N) {
+                const float b = (p.epi == kEpiBiasGelu) ? __half2float(p.bias[n]) : 0.0f;
 #pragma unroll
                 for (int m = 0; m < MP; ++m)
                     if (m < p.M)
-                        p.C[(size_t)m * p.N + n] = __float2half_rn(fmaxf(v[m] * p.alpha, 0.0f));
+                        p.C[(size_t)m * p.N + n] = __float2half_rn(epilogue_value(v[m], p.alpha, b, p.epi));
             }
             pos += kb1 - kb0;
         }

@@ -225,11 +225,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t* src = (j < 4) ? (r0 + 8 * j) : (r1 + 8 * (j - 4));
-                    uint4 v;
-                    v.x = scale_relu_pack(src[0], src[1], p.alpha);
-                    v.y = scale_relu_pack(src[2], src[3], p.alpha);
-                    v.z = scale_relu_pack(src[4], src[5], p.alpha);
-                    v.w = scale_relu_pack(src[6], src[7], p.alpha);
+                    const uint4 v = epilogue_8(src, p.alpha, p.epi, p.bias, n0 + c * 64 + 8 * j, p.N);
                     // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7).
                     *reinterpret_cast<uint4*>(crow + ((j ^ (row & 7)) << 4)) = v;
                 }
@@ -276,7 +272,22 @@ cudaError_t launch_cfg(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
     return cudaGetLastError();
 }
 
+// One thread per output element; only used when K == 0.
+__global__ void gsr_fill_bias_gelu_kernel(__half* C, const __half* bias, int M, int N) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)M * N) return;
+    C[i] = __float2half_rn(gelu_tanh(__half2float(bias[i % N])));
+}
+
 }  // namespace
+
+cudaError_t launch_fill_bias_gelu(__half* C, const __half* bias, int M, int N, cudaStream_t stream) {
+    const long long total = (long long)M * N;
+    const long long blocks = (total + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    gsr_fill_bias_gelu_kernel<<<(unsigned)blocks, 256, 0, stream>>>(C, bias, M, N);
+    return cudaGetLastError();
+}
 
 int tiled_smem_bytes(int bn) { return bn == 256 ? Cfg256::SMEM_BYTES : Cfg128::SMEM_BYTES; }
 

@@ -218,7 +218,14 @@ int choose_path(int64_t M, int64_t N, int num_sms) {
 
 constexpr int kDefaultSms = 152;   // for gsr_select_path before any device is touched
 
+// Which epilogue a call applies, and its bias vector (kEpiBiasGelu only).
+struct Epi {
+    int kind;
+    const __half* bias;
+};
+
 gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
+                    const Epi& ep,
                      cudaStream_t stream, int dev, const DeviceInfo& info) {
     StreamState st;
     gsr_status s = stream_state(dev, stream, 0, 0, &st);
@@ -250,12 +257,15 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
     p.err = st.err;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
+    p.epi = ep.kind;
+    p.bias = ep.bias;
     const int grid = p.num_tiles < info.num_sms ? p.num_tiles : info.num_sms;
     cudaError_t e = gsr::launch_tiled(tmA, tmB, tmC, p, bn, grid, stream);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }
 
 gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
+                    const Epi& ep,
                     cudaStream_t stream, int dev, const DeviceInfo& info) {
     StreamState st;
     gsr_status s = stream_state(dev, stream, 0, 0, &st);
@@ -284,6 +294,8 @@ gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, 
     p.err = st.err;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
+    p.epi = ep.kind;
+    p.bias = ep.bias;
     int clusters = gsr::pair_max_active_clusters();
     if (clusters <= 0) clusters = info.num_sms / 2;
     if (clusters > p.num_tiles) clusters = p.num_tiles;
@@ -292,6 +304,7 @@ gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, 
 }
 
 gsr_status run_skinny(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
+                    const Epi& ep,
                       cudaStream_t stream, int dev, const DeviceInfo& info) {
     const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     const int n_tiles = (N + 127) / 128;
@@ -322,8 +335,33 @@ gsr_status run_skinny(const void* A, const void* B, void* C, int M, int N, int K
     p.err = st.err;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
+    p.epi = ep.kind;
+    p.bias = ep.bias;
     cudaError_t e = gsr::launch_skinny(tmBt, tmAt, p, mp, stream);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+}
+
+// Every entry point that runs the GEMM: validation, K == 0, path choice, launch.
+gsr_status gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                     float alpha, const Epi& ep, CUstream_st* stream) {
+    bool nothing = false;
+    gsr_status s = validate(A, B, C, M, N, K, &nothing);
+    if (s != GSR_OK || nothing) return s;
+    int dev = 0;
+    DeviceInfo info;
+    if ((s = device_info(&dev, &info)) != GSR_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {   // empty sum: every output is the epilogue applied to 0
+        cudaError_t e = (ep.kind == gsr::kEpiBiasGelu)
+                            ? gsr::launch_fill_bias_gelu(static_cast<__half*>(C), ep.bias, (int)M, (int)N, st)
+                            : cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
+        return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+    }
+    if ((s = load_encoder()) != GSR_OK) return s;
+    const int path = choose_path(M, N, info.num_sms);
+    if (path == 1) return run_skinny(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
+    if (path == 2) return run_pair(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
+    return run_tiled(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
 }
 
 }  // namespace
@@ -332,22 +370,26 @@ extern "C" {
 
 gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                            float alpha, CUstream_st* stream) {
-    bool nothing = false;
-    gsr_status s = validate(A, B, C, M, N, K, &nothing);
-    if (s != GSR_OK || nothing) return s;
-    int dev = 0;
-    DeviceInfo info;
-    if ((s = device_info(&dev, &info)) != GSR_OK) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (K == 0) {
-        cudaError_t e = cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
-        return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+    return gemm_impl(A, B, C, M, N, K, alpha, Epi{gsr::kEpiScaleRelu, nullptr}, stream);
+}
+
+gsr_status gemm_scale(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                      float alpha, CUstream_st* stream) {
+    return gemm_impl(A, B, C, M, N, K, alpha, Epi{gsr::kEpiScale, nullptr}, stream);
+}
+
+gsr_status gemm_bias_gelu(const void* A, const void* B, const void* bias, void* C, int64_t M,
+                          int64_t N, int64_t K, CUstream_st* stream) {
+    // the bias vector: present, 16-byte aligned, not overlapping C (sizes are checked later)
+    if (M > 0 && N > 0 && M <= INT_MAX && N <= INT_MAX && C) {
+        if (!bias) return GSR_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(bias) & 15u) return GSR_ERR_ALIGNMENT;
+        const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), c1 = c0 + (uint64_t)M * N * 2;
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(bias), b1 = b0 + (uint64_t)N * 2;
+        if (c0 < b1 && b0 < c1) return GSR_ERR_ALIAS;
     }
-    if ((s = load_encoder()) != GSR_OK) return s;
-    const int path = choose_path(M, N, info.num_sms);
-    if (path == 1) return run_skinny(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
-    if (path == 2) return run_pair(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
-    return run_tiled(A, B, C, (int)M, (int)N, (int)K, alpha, st, dev, info);
+    return gemm_impl(A, B, C, M, N, K, 1.0f, Epi{gsr::kEpiBiasGelu, static_cast<const __half*>(bias)},
+                     stream);
 }
 
 gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* dA, void* dB,
@@ -419,6 +461,8 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
     p.C = static_cast<__half*>(C);
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.test_flags = 0;
+    p.epi = gsr::kEpiScaleRelu;
+    p.bias = nullptr;
     e = gsr::launch_skinny_noalloc(tmBt, tmAt, p, mp, st);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }

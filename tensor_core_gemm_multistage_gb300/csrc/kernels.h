@@ -28,6 +28,13 @@ enum TestFlags : uint32_t {
     kTestNoChunkedB = 2u,       // host: copy B as separate 64-column boxes even when N % 64 == 0
 };
 
+// What the epilogue applies to the fp32 accumulator before the fp16 store.
+enum Epilogue : int {
+    kEpiScaleRelu = 0,   // max(alpha * acc, 0)
+    kEpiScale = 1,       // alpha * acc (alpha = 1: plain GEMM)
+    kEpiBiasGelu = 2,    // GELU(acc + bias[n]), tanh approximation
+};
+
 struct TiledParams {
     int M, N, K;
     float alpha;
@@ -36,6 +43,8 @@ struct TiledParams {
     uint64_t timeout_ns;    // bound on every mbarrier wait
     uint32_t test_flags;
     int b_chunked;          // tmB is the 3-D view {64, K, N/64} of B (N % 64 == 0)
+    int epi;                // Epilogue
+    const __half* bias;     // kEpiBiasGelu: N values, 16-byte aligned
 };
 
 struct SkinnyParams {
@@ -51,6 +60,8 @@ struct SkinnyParams {
     int* err;
     uint64_t timeout_ns;
     uint32_t test_flags;
+    int epi;                // Epilogue
+    const __half* bias;     // kEpiBiasGelu: N values
 };
 
 // Tiled path: persistent, one 128 x BN output tile per CTA iteration.
@@ -77,6 +88,9 @@ cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tm
                                   int mp, cudaStream_t stream);
 size_t noalloc_scratch_bytes();
 size_t noalloc_scratch_need(int num_ctas, int n_tiles, int mp);
+
+// C[m, n] = GELU(bias[n]) for every m: the bias-GELU epilogue of an empty (K == 0) sum.
+cudaError_t launch_fill_bias_gelu(__half* C, const __half* bias, int M, int N, cudaStream_t stream);
 
 // Shared-memory bytes a launch needs (for the one-time attribute set-up).
 int tiled_smem_bytes(int bn);

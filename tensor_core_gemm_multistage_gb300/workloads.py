@@ -79,3 +79,10 @@ def sample_rows(M: int, count: int = 128, seed: int = 1234):
     picked = torch.randperm(M, generator=g)[:n].tolist() if M > 0 else []
     edges = [r for r in (0, 127, 128, M - 1) if 0 <= r < M]
     return sorted(set(picked) | set(edges))
+
+
+def make_bias(N: int, seed: int = 0):
+    """Seeded bias vector for the bias + GELU epilogue: randn(N) * 2 rounded to fp16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return (torch.randn(N, generator=g, dtype=torch.float32) * 2).half().contiguous()

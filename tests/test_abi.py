@@ -124,3 +124,17 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "libgsr.so"))
     with pytest.raises(ImportError):
         binding.lib()
+
+
+def test_bias_gelu_argument_checks_need_no_gpu():
+    p = gsr.gemm_bias_gelu_ptr
+    assert p(A, B, 0, C, 4, 8, 8) == gsr.Status.ERR_INVALID_ARG             # no bias
+    assert p(A, B, 0x300008, C, 4, 8, 8) == gsr.Status.ERR_ALIGNMENT         # bias not 16-byte aligned
+    assert p(A, B, C + 16, C, 4, 8, 8) == gsr.Status.ERR_ALIAS               # bias inside C
+    assert p(A, B, 0, C, 0, 8, 8) == gsr.Status.OK                           # empty output
+
+
+def test_scale_entry_validates_like_the_fused_one():
+    L = gsr.lib()
+    assert L.gemm_scale(A, B, C, -1, 8, 8, ctypes.c_float(1.0), None) == gsr.Status.ERR_INVALID_ARG
+    assert L.gemm_scale(A, B, A, 64, 64, 64, ctypes.c_float(1.0), None) == gsr.Status.ERR_ALIAS

@@ -353,3 +353,98 @@ def test_threads_do_not_change_results():
     finally:
         oracle.set_num_threads(n0)
     assert np.array_equal(c1.view(np.uint16), c2.view(np.uint16))
+
+
+# ----------------------------------------------------------------------------
+# further epilogues: alpha * sum (plain GEMM) and GELU(sum + bias)
+# (aikraft.ru TileLang tutorial survey: make_matmul and make_matmul_bias_gelu sections)
+# ----------------------------------------------------------------------------
+
+def test_epilogue_kind0_is_the_fused_operator():
+    rng = np.random.default_rng(20)
+    A = _rand16(rng, (23, 41))
+    B = _rand16(rng, (41, 19))
+    for alpha in (0.5, -1.25):
+        c0 = oracle.gemm_epilogue(A, B, alpha, oracle.EPI_SCALE_RELU)
+        c1 = oracle.gemm_scale_relu(A, B, alpha)
+        assert np.array_equal(c0.view(np.uint16), c1.view(np.uint16))
+
+
+@pytest.mark.parametrize("alpha", [1.0, 0.5, -0.75])
+def test_scale_identity_b_keeps_negatives(alpha):
+    rng = np.random.default_rng(21)
+    A = _rand16(rng, (37, 24))
+    C = oracle.gemm_epilogue(A, np.eye(24, dtype=np.float16), alpha, oracle.EPI_SCALE)
+    want = (float(np.float32(alpha)) * A.astype(np.float64)).astype(np.float16)
+    assert np.array_equal(C.view(np.uint16), want.view(np.uint16))
+    assert np.any(C < 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 2), (7, 3, 11), (4, 9, 17)])
+def test_scale_brute_force_exact(M, N, K):
+    rng = np.random.default_rng(M * 31 + N + K)
+    A = _rand16(rng, (M, K))
+    B = _rand16(rng, (K, N))
+    alpha = -0.3
+    C = oracle.gemm_epilogue(A, B, alpha, oracle.EPI_SCALE)
+    al = Fraction(float(np.float32(alpha)))
+    for i in range(M):
+        for j in range(N):
+            s = sum((Fraction(float(A[i, k])) * Fraction(float(B[k, j])) for k in range(K)),
+                    Fraction(0))
+            assert C.view(np.uint16)[i, j] == _f16_bits_from_fraction(al * s)
+
+
+def _torch_gelu_tanh(x):
+    import torch
+    return torch.nn.functional.gelu(torch.from_numpy(np.asarray(x, np.float64)),
+                                    approximate="tanh").numpy()
+
+
+def test_gelu_identity_b_matches_torch_gelu():
+    # identity B makes the sum exactly A, so Y = GELU(A + bias) in fp64; torch's own
+    # tanh-form GELU is an independent implementation of the same function
+    rng = np.random.default_rng(22)
+    K = 48
+    A = (rng.standard_normal((40, K)) * 3).astype(np.float16)
+    bias = (rng.standard_normal(K) * 2).astype(np.float16)
+    C, Y = oracle.gemm_epilogue(A, np.eye(K, dtype=np.float16), kind=oracle.EPI_BIAS_GELU,
+                                bias=bias, return_pre=True)
+    x = A.astype(np.float64) + bias.astype(np.float64)[None, :]
+    ref = _torch_gelu_tanh(x)
+    # absolute floor 1e-14: torch's 0.5x(1 + tanh u) cancels to ~1e-16 absolute for x < -7
+    # (far below binary16's smallest subnormal, 6e-8), where the oracle's form does not
+    assert np.allclose(Y, ref, rtol=1e-13, atol=1e-14)
+    assert np.array_equal(C.view(np.uint16), Y.astype(np.float16).view(np.uint16))
+    assert np.any(x < -7)                     # the far negative tail is exercised too
+
+
+def test_gelu_odd_part_identity_and_limits():
+    # tanh-form GELU satisfies GELU(-x) = GELU(x) - x; GELU(0) = 0; GELU(x) -> x, GELU(-x) -> 0
+    vals = np.array([0.0, 0.25, 1.0, 2.5, 7.0, 12.0], dtype=np.float16)
+    K = vals.shape[0]
+    A = np.stack([vals, -vals]).astype(np.float16)            # rows x and -x
+    zero_bias = np.zeros(K, np.float16)
+    _, Y = oracle.gemm_epilogue(A, np.eye(K, dtype=np.float16), kind=oracle.EPI_BIAS_GELU,
+                                bias=zero_bias, return_pre=True)
+    x = vals.astype(np.float64)
+    assert np.allclose(Y[1], Y[0] - x, rtol=0, atol=1e-12)
+    assert Y[0, 0] == 0.0
+    assert abs(Y[0, -1] - 12.0) < 1e-12 and abs(Y[1, -1]) < 1e-12
+
+
+def test_gelu_all_ones_with_bias():
+    # sum = K exactly; Y = GELU(K + bias[n])
+    K, N = 6, 4
+    bias = np.array([-8.0, -6.0, -1.5, 0.5], np.float16)
+    C, Y = oracle.gemm_epilogue(np.ones((3, K), np.float16), np.ones((K, N), np.float16),
+                                kind=oracle.EPI_BIAS_GELU, bias=bias, return_pre=True)
+    ref = _torch_gelu_tanh(K + bias.astype(np.float64))
+    assert np.allclose(Y, ref[None, :], rtol=1e-13, atol=1e-14)
+
+
+def test_gelu_k_zero_is_gelu_of_bias():
+    bias = np.array([-3.0, -0.5, 0.0, 0.5, 3.0, 9.0, -9.0, 1.0], np.float16)
+    C, Y = oracle.gemm_epilogue(np.zeros((2, 0), np.float16), np.zeros((0, 8), np.float16),
+                                kind=oracle.EPI_BIAS_GELU, bias=bias, return_pre=True)
+    assert np.allclose(Y, _torch_gelu_tanh(bias.astype(np.float64))[None, :], rtol=1e-13, atol=1e-14)
