@@ -99,6 +99,12 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job_tflops(world: int, flops_per_rank: float, max_ms: float) -> float:
+    """Replica mode: every rank runs the whole workload, so the job does world x the work in
+    the slowest rank's time."""
+    return world * flops_per_rank / (max_ms * 1e-3) / 1e12
+
+
 def barrier(world: int) -> None:
     if world > 1:
         import torch.distributed as dist
@@ -350,7 +356,7 @@ def run_gsr(args, w):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world)
-        e2e = {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": whole_job_tflops(world, w.flops, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": inputs_bytes, "d2h_bytes_per_step": w.M * w.N * 2,
                "ms_per_step": e2e_ms, "steps": args.e2e_steps}
     if sampler is not None:
@@ -380,7 +386,7 @@ def run_gsr(args, w):
         return 0
 
     peaks, peaks_src = measured_peaks()
-    value = world * w.flops / (step_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, w.flops, step_ms)
     if path == 1:
         achieved = w.bytes / (kernel_avg_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])

@@ -133,8 +133,7 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
  * split-K partial tiles) lives in one fixed 12 MiB array inside the library,
  * which every GPU that loads the library holds until the process exits.
  * Sizes whose scratch would not fit return GSR_ERR_SCRATCH_LIMIT before any
- * work is queued; on a 152-SM GB300 that happens only for N above about
- * 8.3e7 (33 <= M <= 64), 2.4e8 (17 <= M <= 32) or 3.2e8 (M <= 16).
+ * work is queued; on a 152-SM GB300 that happens only for N above about 4.0e8.
  * The call never runs cudaMalloc, cudaFree or any other allocating routine.
  *
  * The first call on a device looks up the array's device address (one-time
@@ -173,6 +172,13 @@ int gsr_select_path(int64_t M, int64_t N, int64_t K);
  * 5 = tiled on CTA pairs with 256 x 256 tiles.
  * For tests and measurements. */
 void gsr_set_path_override(int path);
+
+/* Raster grouping of the tiled kernels (process-wide): `group` consecutive tile rows
+ * (M blocks) share each tile column before moving on, so that concurrently running
+ * CTAs reuse the same A and B panels from L2 -- the "L2 swizzle" knob of the aikraft.ru
+ * TileLang tutorial survey's "Knobs" section (3).  0 restores each kernel's default
+ * (16 for one CTA per tile, 8 for CTA pairs).  For tuning and measurements. */
+void gsr_set_raster_group(int group);
 
 /* Upper bound, in nanoseconds, on every wait inside the kernels (default 1 s).
  * A wait that runs out records an error (see gsr_device_status) and the kernel

@@ -10,7 +10,7 @@ from .binding import (KERNEL_PAIR, KERNEL_SKINNY, KERNEL_TILED, PATH_AUTO, PATH_
                       GsrError, Status, device_status, gemm_bias_gelu, gemm_bias_gelu_ptr,
                       gemm_scale, gemm_scale_relu, gemm_scale_relu_host,
                       gemm_scale_relu_host_ptr, gemm_scale_relu_ptr, last_cuda_error, lib,
-                      library_path, select_path, set_path_override, set_test_flags,
+                      library_path, select_path, set_path_override, set_raster_group, set_test_flags,
                       set_wait_timeout_ns, shutdown, status_string, version)
 from ._build import build
 
@@ -19,6 +19,6 @@ __all__ = [
     "Status", "build", "device_status", "gemm_bias_gelu", "gemm_bias_gelu_ptr", "gemm_scale",
     "gemm_scale_relu", "gemm_scale_relu_host",
     "gemm_scale_relu_host_ptr", "gemm_scale_relu_ptr", "last_cuda_error", "lib", "library_path",
-    "select_path", "set_path_override", "set_test_flags", "set_wait_timeout_ns", "shutdown",
+    "select_path", "set_path_override", "set_raster_group", "set_test_flags", "set_wait_timeout_ns", "shutdown",
     "status_string", "version",
 ]

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.gsr_set_path_override.argtypes = [i32]
         L.gsr_set_wait_timeout_ns.restype = None
         L.gsr_set_wait_timeout_ns.argtypes = [u64]
+        L.gsr_set_raster_group.restype = None
+        L.gsr_set_raster_group.argtypes = [i32]
         L.gsr_set_test_flags.restype = None
         L.gsr_set_test_flags.argtypes = [u32]
         L.gsr_last_cuda_error.restype = i32
@@ -118,6 +120,10 @@ def set_path_override(path: int) -> None:
 
 def set_wait_timeout_ns(ns: int) -> None:
     lib().gsr_set_wait_timeout_ns(int(ns))
+
+
+def set_raster_group(group: int) -> None:
+    lib().gsr_set_raster_group(int(group))
 
 
 def set_test_flags(flags: int) -> None:

@@ -8,14 +8,15 @@
 //    128 columns of C per tile as the MMA's M and M (rounded up to MP = 16/32/64) as
 //    its N.  B^T is read straight from row-major B as an MN-major operand and A^T from
 //    row-major A as a K-major operand: nothing is transposed in memory;
-//  * stream-K: the (tile, 64-wide k block) units are laid out tile-major and CTA p of
-//    P owns the contiguous run [p*T/P, (p+1)*T/P), so every SM streams the same number
-//    of B bytes.  A run that covers a whole tile stores it directly; a run that covers
-//    part of a tile writes an fp32 partial into its own slot of the workspace and takes
-//    a ticket; the CTA whose ticket completes the tile's k count sums the partials in
-//    fixed CTA order (deterministic), applies scale + ReLU + fp16 and resets the
-//    ticket to 0 for the next launch.  Nobody waits on another CTA, so nothing can
-//    deadlock across CTAs.
+//  * split K into S equal slabs per tile (S = #SMs / #tiles, at least 1): work item w =
+//    (slab w / T, tile w % T) for T tiles, so the CTAs running at one time work on the
+//    same slab and walk through the same rows of B in step, as one streaming pass (DRAM
+//    pages are read whole); with S == 1 each item is a whole tile and is stored directly.
+//    With S > 1 each item writes an fp32 partial tile into its own slot (tile, slab) of
+//    the workspace and takes a ticket; the CTA that takes the S-th ticket sums the S
+//    partials in slab order (deterministic), applies the epilogue and resets the ticket to
+//    0 for the next launch.  Nobody waits on another CTA, so nothing can deadlock across
+//    CTAs.
 #include <atomic>
 
 #include "device_common.cuh"
@@ -49,19 +50,11 @@ struct SkinnyCfg {
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
 };
 
-// Owner of unit x when CTA p owns [floor(p*T/P), floor((p+1)*T/P)).
-__device__ __forceinline__ int unit_owner(long long x, long long T, int P) {
-    return (int)(((x + 1) * (long long)P + T - 1) / T) - 1;
-}
-__device__ __forceinline__ long long cta_begin(int p, long long T, int P) {
-    return (long long)p * T / P;
-}
-
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gsr_skinny_kernel(const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmAt,
                       const SkinnyParams p) {
-    constexpr int S = Cfg::STAGES;
+    constexpr int NS = Cfg::STAGES;
     constexpr int MP = Cfg::MP;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -69,24 +62,23 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t sb = smem_u32(smem);
 
     auto full_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * s; };
-    auto empty_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (S + s); };
-    auto tfull_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + a); };
-    auto tempty_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + 2 + a); };
-    const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * S + 4);
+    auto empty_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (NS + s); };
+    auto tfull_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * NS + a); };
+    auto tempty_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * NS + 2 + a); };
+    const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * NS + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 4);
     volatile int* s_last = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long long T = p.total_units;
-    const int P = p.num_ctas;
     const int kbpt = p.num_k_blocks;
-    const long long my_begin = cta_begin(blockIdx.x, T, P);
-    const long long my_end = cta_begin(blockIdx.x + 1, T, P);
+    const int n_tiles = p.num_n_tiles;
+    const int S = p.num_slabs;
+    const int W = n_tiles * S;                 // work items, slab-major
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -122,10 +114,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             uint32_t armed_mask = 0, armed_parity = 0;
             bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
             bool ok = true;
-            for (long long pos = my_begin; ok && pos < my_end;) {
-                const int tile = (int)(pos / kbpt);
-                const int kb0 = (int)(pos % kbpt);
-                const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+            for (int item = blockIdx.x; ok && item < W; item += gridDim.x) {
+                const int tile = item % n_tiles, slab = item / n_tiles;
+                const int kb0 = slab * kbpt / S, kb1 = (slab + 1) * kbpt / S;
                 const int n0 = tile * Cfg::TN;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
@@ -146,11 +137,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         armed_mask |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if (++stage == NS) { stage = 0; phase ^= 1u; }
                 }
-                pos += kb1 - kb0;
             }
-            for (int s = 0; s < S; ++s)
+            for (int s = 0; s < NS; ++s)
                 if (armed_mask & (1u << s)) w.drain(full_bar(s), (armed_parity >> s) & 1u);
         }
         __syncwarp();
@@ -159,9 +149,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true;
-            for (long long pos = my_begin; ok && pos < my_end; ++it) {
-                const int kb0 = (int)(pos % kbpt);
-                const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+            for (int item = blockIdx.x; ok && item < W; item += gridDim.x, ++it) {
+                const int slab = item / n_tiles;
+                const int kb0 = slab * kbpt / S, kb1 = (slab + 1) * kbpt / S;
                 const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
                 if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
                 tcgen05_fence_after();
@@ -183,11 +173,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         mma_f16_ss(d_tmem, ad, bd, Cfg::IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if (++stage == NS) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit(tfull_bar(acc));
-                pos += kb1 - kb0;
             }
             mma_commit(drain_bar);
             w.drain(drain_bar, 0);
@@ -199,10 +188,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int nl = quad * 32 + lane;     // column of C inside the tile == TMEM lane
         const int et = threadIdx.x - 64;
         uint32_t it = 0;
-        for (long long pos = my_begin; pos < my_end; ++it) {
-            const int tile = (int)(pos / kbpt);
-            const int kb0 = (int)(pos % kbpt);
-            const int kb1 = (int)min((long long)kbpt, kb0 + (my_end - pos));
+        for (int item = blockIdx.x; item < W; item += gridDim.x, ++it) {
+            const int tile = item % n_tiles, slab = item / n_tiles;
             const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
             const bool got = w.wait(tfull_bar(acc), acc_parity, kDevErrEpilogueFull);
             if (!named_bar_and(1, 128, got)) break;
@@ -225,37 +212,31 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
             const int n = tile * Cfg::TN + nl;
             bool store = true;
-            if (!(kb0 == 0 && kb1 == kbpt)) {
-                // Part of a tile: publish the partial, take a ticket.
-                const int slot = (pos == my_begin) ? 0 : 1;
-                float* mine = p.partials + ((size_t)blockIdx.x * 2 + slot) * (MP * Cfg::TN);
+            if (S > 1) {
+                // One slab of a tile: publish the partial, take a ticket.
+                float* mine = p.partials + ((size_t)tile * S + slab) * (MP * Cfg::TN);
 #pragma unroll
                 for (int m = 0; m < MP; ++m) mine[m * Cfg::TN + nl] = v[m];
                 __threadfence();
                 named_bar_sync(1, 128);
                 if (et == 0) {
-                    const int add = kb1 - kb0;
-                    const int old = atomicAdd(p.tickets + tile, add);
-                    *s_last = (old + add == kbpt) ? 1 : 0;
+                    const int old = atomicAdd(p.tickets + tile, 1);
+                    *s_last = (old + 1 == S) ? 1 : 0;
                 }
                 named_bar_sync(1, 128);
                 store = (*s_last != 0);
                 if (store) {
-                    // Last contributor: sum every partial of this tile in CTA order.
+                    // Last slab to finish: sum the tile's partials in slab order.
                     __threadfence();
-                    const long long u0 = (long long)tile * kbpt;
-                    const int p_first = unit_owner(u0, T, P);
-                    const int p_last = unit_owner(u0 + kbpt - 1, T, P);
                     float sum[MP];
 #pragma unroll
                     for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
-                    for (int q = p_first; q <= p_last; ++q) {
-                        if (q == (int)blockIdx.x) {
+                    for (int q = 0; q < S; ++q) {
+                        if (q == slab) {
 #pragma unroll
                             for (int m = 0; m < MP; ++m) sum[m] += v[m];
                         } else {
-                            const int qslot = (cta_begin(q, T, P) >= u0) ? 0 : 1;
-                            const float* src = p.partials + ((size_t)q * 2 + qslot) * (MP * Cfg::TN);
+                            const float* src = p.partials + ((size_t)tile * S + q) * (MP * Cfg::TN);
 #pragma unroll
                             for (int m = 0; m < MP; ++m) sum[m] += __ldcg(src + m * Cfg::TN + nl);
                         }
@@ -272,7 +253,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     if (m < p.M)
                         p.C[(size_t)m * p.N + n] = __float2half_rn(epilogue_value(v[m], p.alpha, b, p.epi));
             }
-            pos += kb1 - kb0;
         }
     }
 
@@ -355,9 +335,10 @@ size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
 // Byte layout inside the array: [0, 256) error word, [256, 256 + tickets) tickets rounded up
 // to 256 bytes, then the partial tiles.
-size_t noalloc_scratch_need(int num_ctas, int n_tiles, int mp) {
+size_t noalloc_scratch_need(int n_tiles, int slabs, int mp) {
     const size_t tickets = ((size_t)n_tiles * sizeof(int) + 255) / 256 * 256;
-    return 256 + tickets + (size_t)num_ctas * 2 * mp * 128 * sizeof(float);
+    const size_t slots = slabs > 1 ? (size_t)n_tiles * slabs : 0;
+    return 256 + tickets + slots * mp * 128 * sizeof(float);
 }
 
 cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tmAt, SkinnyParams p,
@@ -381,7 +362,7 @@ cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tm
         }
         base = base_of[dev];
     }
-    if (noalloc_scratch_need(p.num_ctas, p.num_n_tiles, mp) > kNoAllocScratchBytes)
+    if (noalloc_scratch_need(p.num_n_tiles, p.num_slabs, mp) > kNoAllocScratchBytes)
         return cudaErrorInvalidValue;
     unsigned char* b = static_cast<unsigned char*>(base);
     const size_t tickets = ((size_t)p.num_n_tiles * sizeof(int) + 255) / 256 * 256;

@@ -23,6 +23,7 @@ thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_path_override{0};
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<uint32_t> g_test_flags{0};
+std::atomic<int> g_raster_group{0};   // 0: each kernel's default grouping
 
 constexpr int kSkinnyMaxM = 64;
 constexpr int kGroupM = 16;
@@ -253,6 +254,7 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
     p.num_k_blocks = kb;
     p.num_tiles = mb * nb;
     p.group_m = kGroupM;
+    if (const int g = g_raster_group.load(std::memory_order_relaxed)) p.group_m = g;
     p.b_chunked = 0;
     p.err = st.err;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
@@ -291,6 +293,7 @@ gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, 
     p.num_k_blocks = (K + 63) / 64;
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.group_m = kGroupM / 2;
+    if (const int g = g_raster_group.load(std::memory_order_relaxed)) p.group_m = g;
     p.err = st.err;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
@@ -309,11 +312,12 @@ gsr_status run_skinny(const void* A, const void* B, void* C, int M, int N, int K
     const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     const int n_tiles = (N + 127) / 128;
     const int kbpt = (K + 63) / 64;
-    const long long T = (long long)n_tiles * kbpt;
-    const int P = (int)(T < info.num_sms ? T : info.num_sms);
+    int S = 1, P = 1;
+    gsr::skinny_split(n_tiles, kbpt, info.num_sms, &S, &P);
 
     StreamState st;
-    gsr_status s = stream_state(dev, stream, (size_t)P * 2 * mp * 128, (size_t)n_tiles, &st);
+    const size_t partial_floats = S > 1 ? (size_t)n_tiles * S * mp * 128 : 0;
+    gsr_status s = stream_state(dev, stream, partial_floats, (size_t)n_tiles, &st);
     if (s != GSR_OK) return s;
 
     CUtensorMap tmBt, tmAt;
@@ -327,7 +331,7 @@ gsr_status run_skinny(const void* A, const void* B, void* C, int M, int N, int K
     p.alpha = alpha;
     p.num_n_tiles = n_tiles;
     p.num_k_blocks = kbpt;
-    p.total_units = T;
+    p.num_slabs = S;
     p.num_ctas = P;
     p.partials = st.partials;
     p.tickets = st.tickets;
@@ -434,9 +438,9 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
     const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     const int n_tiles = (int)((N + 127) / 128);
     const int kbpt = (int)((K + 63) / 64);
-    const long long T = (long long)n_tiles * (kbpt > 0 ? kbpt : 1);
-    const int P = (int)(T < sms ? T : sms);
-    if (gsr::noalloc_scratch_need(P, n_tiles, mp) > gsr::noalloc_scratch_bytes())
+    int S = 1, P = 1;
+    gsr::skinny_split(n_tiles, kbpt > 0 ? kbpt : 1, sms, &S, &P);
+    if (gsr::noalloc_scratch_need(n_tiles, S, mp) > gsr::noalloc_scratch_bytes())
         return GSR_ERR_SCRATCH_LIMIT;
     if (K == 0) {
         e = cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
@@ -453,7 +457,7 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
     p.alpha = alpha;
     p.num_n_tiles = n_tiles;
     p.num_k_blocks = kbpt;
-    p.total_units = T;
+    p.num_slabs = S;
     p.num_ctas = P;
     p.partials = nullptr;   // filled from the fixed array by the launch
     p.tickets = nullptr;
@@ -512,6 +516,8 @@ void gsr_set_path_override(int path) { g_path_override.store(path, std::memory_o
 void gsr_set_wait_timeout_ns(uint64_t ns) {
     g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed);
 }
+
+void gsr_set_raster_group(int group) { g_raster_group.store(group > 0 ? group : 0, std::memory_order_relaxed); }
 
 void gsr_set_test_flags(uint32_t flags) { g_test_flags.store(flags, std::memory_order_relaxed); }
 

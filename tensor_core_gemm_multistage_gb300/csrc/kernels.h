@@ -52,9 +52,9 @@ struct SkinnyParams {
     float alpha;
     int num_n_tiles;        // ceil(N / 128)
     int num_k_blocks;       // ceil(K / 64) per tile
-    long long total_units;  // num_n_tiles * num_k_blocks
-    int num_ctas;           // P: CTA p owns units [p*T/P, (p+1)*T/P)
-    float* partials;        // [num_ctas][2][MP][128] fp32 split-K partial tiles
+    int num_slabs;          // S: each tile's k blocks are split into S equal slabs
+    int num_ctas;           // grid: min(num_n_tiles * S, #SMs), items strided by the grid
+    float* partials;        // S > 1: [num_n_tiles][S][MP][128] fp32 partial tiles
     int* tickets;           // [num_n_tiles], zero between launches
     __half* C;              // (M, N) row-major output
     int* err;
@@ -63,6 +63,17 @@ struct SkinnyParams {
     int epi;                // Epilogue
     const __half* bias;     // kEpiBiasGelu: N values
 };
+
+// Split of the small-M work: S slabs per tile so that n_tiles * S fills the SMs once (each
+// slab at least one k block), grid = min(n_tiles * S, sms).
+inline void skinny_split(int n_tiles, int k_blocks, int sms, int* slabs, int* ctas) {
+    int S = n_tiles >= sms ? 1 : sms / n_tiles;
+    if (S > k_blocks) S = k_blocks;
+    if (S < 1) S = 1;
+    const long long items = (long long)n_tiles * S;
+    *slabs = S;
+    *ctas = (int)(items < sms ? items : sms);
+}
 
 // Tiled path: persistent, one 128 x BN output tile per CTA iteration.
 // bn is 128 or 256.  grid = min(num_tiles, num_sms).
@@ -76,7 +87,7 @@ cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
 int pair_max_active_clusters();
 int pair_smem_bytes();
 
-// Skinny path (M <= 64): C^T = B^T A^T on 128-row tiles of N, stream-K split of K.
+// Skinny path (M <= 64): C^T = B^T A^T on 128-row tiles of N, K split into slabs.
 // mp is the MMA N (16, 32 or 64).
 cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
                           int mp, cudaStream_t stream);
@@ -87,7 +98,7 @@ cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, cons
 cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tmAt, SkinnyParams p,
                                   int mp, cudaStream_t stream);
 size_t noalloc_scratch_bytes();
-size_t noalloc_scratch_need(int num_ctas, int n_tiles, int mp);
+size_t noalloc_scratch_need(int n_tiles, int slabs, int mp);
 
 // C[m, n] = GELU(bias[n]) for every m: the bias-GELU epilogue of an empty (K == 0) sum.
 cudaError_t launch_fill_bias_gelu(__half* C, const __half* bias, int M, int N, cudaStream_t stream);

@@ -1,0 +1,127 @@
+"""Knob sweep: time every runtime configuration of the library on one shape.
+
+The aikraft.ru TileLang tutorial survey ("Knobs" section, 3) tunes a tiled matmul by
+trying block sizes, pipeline depth and an L2-swizzle flag, keeping the fastest
+configuration that fits in shared memory.  Here tile shapes and pipeline depths are fixed
+per kernel at compile time (each kernel's shared-memory budget is checked by a
+static_assert), so the runtime knobs are:
+
+  kernel   tiled 128x256, tiled 128x128, CTA pair 256x256, small-M (M <= 64 only)
+  raster   the grouping of tile rows for L2 reuse (gsr_set_raster_group)
+  b_copy   one 3-D copy per stage for B, or two 2-D boxes (CTA-pair kernel, N % 64 == 0)
+
+    python -m tensor_core_gemm_multistage_gb300.sweep --M 8192 --N 8192 --K 8192
+
+prints one JSON line per configuration and a last line naming the fastest one and the
+kernel the library picks on its own.  Timing: CUDA events around back-to-back calls after
+warm-up, as the tutorial's benchmark_op does; every configuration is timed in several
+rounds of shuffled order and the median is kept.  A development tool; nothing here changes the
+library's defaults.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import sys
+
+from . import binding as gsr
+
+KERNELS = {"tiled_128x256": gsr.PATH_TILED_256, "tiled_128x128": gsr.PATH_TILED_128,
+           "pair_256x256": gsr.PATH_PAIR, "small_m": gsr.PATH_SKINNY}
+RASTERS = (0, 4, 16)     # 0: the kernel's default grouping
+NO_3D_B = 2              # test flag bit 1
+
+
+def candidates(M: int, N: int, K: int):
+    """Every (kernel, raster, b_copy) combination that is valid for this shape."""
+    out = []
+    for name, path in KERNELS.items():
+        if name == "small_m" and M > 64:
+            continue
+        rasters = (0,) if name == "small_m" else RASTERS
+        copies = ("3d", "2d") if (name == "pair_256x256" and N % 64 == 0) else ("default",)
+        for r in rasters:
+            for c in copies:
+                out.append({"kernel": name, "path": path, "raster": r, "b_copy": c})
+    return out
+
+
+def time_config(cfg, A, B, C, alpha, warmup=5, iters=30):
+    import torch
+    gsr.set_path_override(cfg["path"])
+    gsr.set_raster_group(cfg["raster"])
+    gsr.set_test_flags(NO_3D_B if cfg["b_copy"] == "2d" else 0)
+    try:
+        for _ in range(warmup):
+            gsr.gemm_scale_relu(A, B, C, alpha)
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(iters):
+            gsr.gemm_scale_relu(A, B, C, alpha)
+        e.record()
+        torch.cuda.synchronize()
+        status, code = gsr.device_status()
+        if status != gsr.Status.OK:
+            raise RuntimeError("device status %s (%#x)" % (status.name, code))
+        return s.elapsed_time(e) / iters
+    finally:
+        gsr.set_path_override(gsr.PATH_AUTO)
+        gsr.set_raster_group(0)
+        gsr.set_test_flags(0)
+
+
+def sweep(M: int, N: int, K: int, alpha: float = 0.5, warmup: int = 5, iters: int = 30, seed=0,
+          rounds: int = 3):
+    """Time every candidate `rounds` times, each round in a fresh random order, and keep the
+    median: under the GPU's power cap a configuration timed right after a cool-down runs at a
+    higher clock, so a fixed order would favour whichever comes first."""
+    import random
+    import statistics
+
+    import torch
+    from .workloads import make_inputs
+    A, B = make_inputs(M, N, K, seed=seed)
+    dA, dB = A.cuda(), B.cuda()
+    dC = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    cands = candidates(M, N, K)
+    times = [[] for _ in cands]
+    order = list(range(len(cands)))
+    rng = random.Random(seed)
+    for _ in range(rounds):
+        rng.shuffle(order)
+        for i in order:
+            times[i].append(time_config(cands[i], dA, dB, dC, alpha, warmup, iters))
+    results = []
+    for cfg, ts in zip(cands, times):
+        ms = statistics.median(ts)
+        r = {k: v for k, v in cfg.items() if k != "path"}
+        r.update({"M": M, "N": N, "K": K, "ms": ms, "ms_all": ts,
+                  "TFLOP/s": 2.0 * M * N * K / (ms * 1e-3) / 1e12})
+        results.append(r)
+    best = min(results, key=lambda r: r["ms"])
+    auto = {0: "tiled", 1: "small_m", 2: "pair_256x256"}[gsr.select_path(M, N, K)]
+    return results, best, auto
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description="time every runtime configuration on one shape")
+    ap.add_argument("--M", type=int, required=True)
+    ap.add_argument("--N", type=int, required=True)
+    ap.add_argument("--K", type=int, required=True)
+    ap.add_argument("--alpha", type=float, default=0.5)
+    ap.add_argument("--iters", type=int, default=30)
+    ap.add_argument("--rounds", type=int, default=3)
+    args = ap.parse_args(argv)
+    gsr.lib()
+    results, best, auto = sweep(args.M, args.N, args.K, args.alpha, iters=args.iters,
+                                rounds=args.rounds)
+    for r in results:
+        print(json.dumps(r))
+    print(json.dumps({"best": best, "library_choice": auto}))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -61,7 +61,7 @@ def test_noalloc_rejects_what_it_cannot_hold():
     L = gsr.lib()
     vp = ctypes.c_void_p
     A, B, C = vp(0x10000), vp(1 << 36), vp(1 << 40)   # never touched: rejected first
-    s = L.gemm_scale_relu_noalloc(A, B, C, 64, 1 << 27, 8, ctypes.c_float(1.0),
+    s = L.gemm_scale_relu_noalloc(A, B, C, 64, 1 << 29, 8, ctypes.c_float(1.0),
                                   vp(stream.cuda_stream))
     assert s == gsr.Status.ERR_SCRATCH_LIMIT
     s = L.gemm_scale_relu_noalloc(A, B, C, 65, 64, 8, ctypes.c_float(1.0), vp(stream.cuda_stream))
