@@ -107,6 +107,35 @@ gsr_status gemm_bias_gelu(const void* A, const void* B, const void* bias, void* 
                           int64_t N, int64_t K, struct CUstream_st* stream);
 
 /*
+ * Attention forward, FlashAttention style:
+ *
+ *     O = softmax( softmax_scale * Q K^T  [causal mask] ) V        per batch and head
+ *
+ * (aikraft.ru TileLang tutorial survey "TileLang: создание высокопроизводительных
+ * GPU-ядер", section 6 "FlashAttention: Слияние внимания": online softmax with running
+ * maxima, normalisation sums and rescaling factors, causal masks, pipelined copies.)
+ *
+ *   Q      device pointer, (batch, heads, seq_q, head_dim) float16, row-major.
+ *   K, V   device pointers, (batch, heads, seq_kv, head_dim) float16, row-major.
+ *   O      device pointer, (batch, heads, seq_q, head_dim) float16; written.
+ *   lse    optional device pointer (NULL: not written), (batch, heads, seq_q) float32:
+ *          the natural-log log-sum-exp of each query's scaled, masked scores.
+ *   head_dim        64 or 128.
+ *   softmax_scale   0 selects 1/sqrt(head_dim).
+ *   causal          nonzero: query i keeps key j only when j <= i + (seq_kv - seq_q)
+ *                   (lower triangle aligned to the bottom-right corner).
+ * Scores and softmax in fp32, P rounded to fp16 for the second product, output rounded
+ * once to fp16.  A query with no key left (causal with seq_q > seq_kv, or seq_kv == 0)
+ * gets O = 0 and lse = -inf.  All pointers 16-byte aligned (lse 4-byte); O and lse must
+ * not overlap the inputs or each other.  Caller-owned buffers; asynchronous on `stream`;
+ * errors as for gemm_scale_relu.
+ */
+gsr_status flash_attention_fwd(const void* Q, const void* K, const void* V, void* O, float* lse,
+                               int64_t batch, int64_t heads, int64_t seq_q, int64_t seq_kv,
+                               int64_t head_dim, float softmax_scale, int causal,
+                               struct CUstream_st* stream);
+
+/*
  * gemm_scale_relu with the operands in host memory: copies A and B host ->
  * device into the caller's device buffers dA and dB, runs gemm_scale_relu
  * into dC and copies C back device -> host, all queued on `stream`.  The host

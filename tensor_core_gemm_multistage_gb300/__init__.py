@@ -7,7 +7,8 @@ and 3.
 """
 from .binding import (KERNEL_PAIR, KERNEL_SKINNY, KERNEL_TILED, PATH_AUTO, PATH_PAIR,
                       PATH_SKINNY, PATH_TILED, PATH_TILED_128, PATH_TILED_256,
-                      GsrError, Status, device_status, gemm_bias_gelu, gemm_bias_gelu_ptr,
+                      GsrError, Status, device_status, flash_attention_fwd, gemm_bias_gelu,
+                      gemm_bias_gelu_ptr,
                       gemm_scale, gemm_scale_relu, gemm_scale_relu_host,
                       gemm_scale_relu_host_ptr, gemm_scale_relu_ptr, last_cuda_error, lib,
                       library_path, select_path, set_path_override, set_raster_group, set_test_flags,
@@ -16,7 +17,7 @@ from ._build import build
 
 __all__ = [
     "KERNEL_PAIR", "KERNEL_SKINNY", "KERNEL_TILED", "PATH_AUTO", "PATH_PAIR", "PATH_SKINNY", "PATH_TILED", "PATH_TILED_128", "PATH_TILED_256", "GsrError",
-    "Status", "build", "device_status", "gemm_bias_gelu", "gemm_bias_gelu_ptr", "gemm_scale",
+    "Status", "build", "device_status", "flash_attention_fwd", "gemm_bias_gelu", "gemm_bias_gelu_ptr", "gemm_scale",
     "gemm_scale_relu", "gemm_scale_relu_host",
     "gemm_scale_relu_host_ptr", "gemm_scale_relu_ptr", "last_cuda_error", "lib", "library_path",
     "select_path", "set_path_override", "set_raster_group", "set_test_flags", "set_wait_timeout_ns", "shutdown",

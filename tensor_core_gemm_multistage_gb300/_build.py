@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libgsr.so")
 
-SOURCES = ["gsr_api.cu", "gemm_tiled.cu", "gemm_pair.cu", "gemm_skinny.cu"]
+SOURCES = ["gsr_api.cu", "gemm_tiled.cu", "gemm_pair.cu", "gemm_skinny.cu", "attention_fwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-I" + CSRC]

@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_scale.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
         L.gemm_bias_gelu.restype = i32
         L.gemm_bias_gelu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+        L.flash_attention_fwd.restype = i32
+        L.flash_attention_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
         L.gemm_scale_relu_noalloc.restype = i32
         L.gemm_scale_relu_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
         L.gemm_scale_relu_host.restype = i32
@@ -244,6 +246,37 @@ def gemm_bias_gelu_ptr(A: int, B: int, bias: int, C: int, M: int, N: int, K: int
                        stream: int = 0) -> int:
     return lib().gemm_bias_gelu(A or None, B or None, bias or None, C or None, M, N, K,
                                 stream or None)
+
+
+def flash_attention_fwd(Q, K, V, O, lse=None, softmax_scale: float = 0.0, causal: bool = False,
+                        stream=None):
+    """O = softmax(scale * Q K^T [causal]) V for fp16 CUDA tensors Q (B,H,Sq,D), K and V
+    (B,H,Skv,D), O (B,H,Sq,D); D in {64, 128}; scale 0 means 1/sqrt(D).  ``lse``: optional
+    float32 (B,H,Sq) receiving the log-sum-exp of the scaled scores."""
+    import torch
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float16 or t.dim() != 4 \
+                or not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError("%s must be a contiguous 4-D float16 CUDA tensor" % name)
+    B, H, Sq, D = Q.shape
+    Skv = K.shape[2]
+    if tuple(K.shape) != (B, H, Skv, D) or tuple(V.shape) != (B, H, Skv, D) \
+            or tuple(O.shape) != (B, H, Sq, D):
+        raise ValueError("shapes: Q %s K %s V %s O %s" % (tuple(Q.shape), tuple(K.shape),
+                                                            tuple(V.shape), tuple(O.shape)))
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 (B, H, Sq) tensor")
+    dev = O.device
+    with torch.cuda.device(dev):
+        s = lib().flash_attention_fwd(Q.data_ptr() or None, K.data_ptr() or None,
+                                      V.data_ptr() or None, O.data_ptr() or None,
+                                      lse.data_ptr() if lse is not None else None,
+                                      B, H, Sq, Skv, D, ctypes.c_float(softmax_scale),
+                                      1 if causal else 0, _stream_handle(stream, dev) or None)
+    if s != Status.OK:
+        raise GsrError(s, "flash_attention_fwd")
+    return O
 
 
 def gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, alpha: float, stream=None):

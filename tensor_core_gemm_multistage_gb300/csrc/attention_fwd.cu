@@ -1,0 +1,397 @@
+// attention_fwd.cu - attention forward on sm_103a:  O = softmax(scale * Q K^T [causal]) V.
+//
+// The FlashAttention kernel of the aikraft.ru TileLang tutorial survey ("TileLang: создание
+// высокопроизводительных GPU-ядер", section 6 "FlashAttention: Слияние внимания"): tiles of
+// queries, keys and values, no materialised score matrix, online softmax (running row
+// maxima, normalisation sums, rescaling factors), causal masking, copies pipelined with the
+// matrix products.  Its thread roles follow "TileLang异步协作终极指南" (producers load K/V, one
+// role computes QK^T, another the softmax and the output), rebuilt on tcgen05:
+//
+//  * one CTA per (128-query tile, batch x head); 192 threads: warp 0 issues TMA copies (Q
+//    once, then K_j and V_j into a 2-stage ring), warp 1 issues every MMA from one lane,
+//    warps 2-5 run the softmax, one query row per thread (TMEM lane = row);
+//  * S_j = Q K_j^T (M 128 queries, N 128 keys, K = head_dim) accumulates in TMEM, two
+//    buffers, so S_{j+1} is computed while the softmax reads S_j;
+//  * the softmax reads its S row twice from TMEM (max, then exponentials), writes P_j in
+//    fp16 to 128-byte-swizzled shared memory, and keeps the running max m, sum l and the
+//    output row O in fp32 registers;
+//  * PV_j = P_j V_j (K = 128 keys, N = head_dim, V read as an MN-major operand) lands in a
+//    second pair of TMEM buffers; the softmax merges it as O = alpha_j O + PV_j with
+//    alpha_j = exp2(m_{j-1} - m_j), and at the end divides by l.
+// All waits are bounded (device_common.cuh); nothing traps.
+#include <atomic>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace gsr {
+namespace {
+
+template <int D_>
+struct AttnCfg {
+    static constexpr int D = D_;                      // head dim: 64 or 128
+    static constexpr int BQ = 128, BKV = 128;
+    static constexpr int DCH = D / 64;                // 64-column (128-byte) chunks per row
+    static constexpr int CHUNK_BYTES = 128 * 128;     // one 128-row chunk: 16 KB
+    static constexpr int Q_BYTES = BQ * D * 2;
+    static constexpr int KV_BYTES = BKV * D * 2;
+    static constexpr int P_BYTES = BQ * BKV * 2;      // 32 KB: two 64-key chunks
+    static constexpr int NUM_THREADS = 192;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+    static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int NUM_BARS = 1 + 9 * 2 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int TMEM_COLS = 512;             // S 2 x 128, PV 2 x D
+    static constexpr uint32_t T_S = 0, T_PV = 256;
+    static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q, K both K-major
+    static constexpr uint32_t IDESC_PV = idesc_f16_f32(BQ, D, false, true);     // P K-major, V MN-major
+
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
+    static_assert(T_PV + 2 * D <= TMEM_COLS, "TMEM budget");
+};
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
+    gsr_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    constexpr int D = Cfg::D;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+
+    // barriers: 0 qfull | 1+s kfull | 3+s kempty | 5+s vfull | 7+s vempty | 9+s sfull |
+    //           11+s sempty | 13+s pfull | 15+s pvfull | 17+s pvempty | 19 drain
+    auto bar = [&](int i) { return sb + Cfg::OFF_BAR + 8u * i; };
+    const uint32_t qfull = bar(0), drain = bar(19);
+    auto kfull = [&](int s) { return bar(1 + s); };
+    auto kempty = [&](int s) { return bar(3 + s); };
+    auto vfull = [&](int s) { return bar(5 + s); };
+    auto vempty = [&](int s) { return bar(7 + s); };
+    auto sfull = [&](int s) { return bar(9 + s); };
+    auto sempty = [&](int s) { return bar(11 + s); };
+    auto pfull = [&](int s) { return bar(13 + s); };
+    auto pvfull = [&](int s) { return bar(15 + s); };
+    auto pvempty = [&](int s) { return bar(17 + s); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_qt = (p.Sq + Cfg::BQ - 1) / Cfg::BQ;
+    const int qt = blockIdx.x % n_qt;
+    const int bh = blockIdx.x / n_qt;
+    const int q0 = qt * Cfg::BQ;
+    // key tiles this query tile needs (causal: keys k <= q + offset only)
+    int kv_end = p.Skv;
+    if (p.causal) kv_end = min(p.Skv, q0 + Cfg::BQ + p.causal_offset);
+    const int nkv = kv_end > 0 ? (kv_end + Cfg::BKV - 1) / Cfg::BKV : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(qfull, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(kfull(s), 1);
+            mbar_init(kempty(s), 1);
+            mbar_init(vfull(s), 1);
+            mbar_init(vempty(s), 1);
+            mbar_init(sfull(s), 1);
+            mbar_init(sempty(s), 128);
+            mbar_init(pfull(s), 128);
+            mbar_init(pvfull(s), 1);
+            mbar_init(pvempty(s), 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish_alloc_permit();
+    }
+    tcgen05_fence_before();
+    __syncthreads();
+    tcgen05_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const Waiter w{p.err, p.timeout_ns, abort_flag, kDevErrKernelAttention};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && nkv > 0) {
+            const uint64_t pol = l2_policy_evict_last();   // K and V are read by every query tile
+            uint32_t armed = 0, armed_parity = 0;          // bit 0 Q, bits 1-2 K, bits 3-4 V
+            const bool drop_q = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+            if (!drop_q) {
+                mbar_arrive_expect_tx(qfull, Cfg::Q_BYTES);
+#pragma unroll
+                for (int c = 0; c < Cfg::DCH; ++c)
+                    tma_load_3d(sb + Cfg::OFF_Q + c * Cfg::CHUNK_BYTES, &tmQ, qfull, c * 64, q0, bh, pol);
+                armed |= 1u;
+            }
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1u;
+                if (!w.wait(kempty(s), ph ^ 1u, kDevErrProducerEmpty)) break;
+                mbar_arrive_expect_tx(kfull(s), Cfg::KV_BYTES);
+#pragma unroll
+                for (int c = 0; c < Cfg::DCH; ++c)
+                    tma_load_3d(sb + Cfg::OFF_K + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmK, kfull(s),
+                                c * 64, j * Cfg::BKV, bh, pol);
+                armed |= 2u << s;
+                armed_parity = (armed_parity & ~(2u << s)) | (ph << (1 + s));
+                if (!w.wait(vempty(s), ph ^ 1u, kDevErrProducerEmpty)) break;
+                mbar_arrive_expect_tx(vfull(s), Cfg::KV_BYTES);
+#pragma unroll
+                for (int c = 0; c < Cfg::DCH; ++c)
+                    tma_load_3d(sb + Cfg::OFF_V + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmV, vfull(s),
+                                c * 64, j * Cfg::BKV, bh, pol);
+                armed |= 8u << s;
+                armed_parity = (armed_parity & ~(8u << s)) | (ph << (3 + s));
+            }
+            // every copy started must land before the CTA may exit
+            if (armed & 1u) w.drain(qfull, 0);
+            for (int s = 0; s < 2; ++s) {
+                if (armed & (2u << s)) w.drain(kfull(s), (armed_parity >> (1 + s)) & 1u);
+                if (armed & (8u << s)) w.drain(vfull(s), (armed_parity >> (3 + s)) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && nkv > 0) {
+            bool ok = w.wait(qfull, 0, kDevErrMmaFull);
+            for (int j = 0; ok && j <= nkv; ++j) {
+                if (j < nkv) {
+                    // S_j = Q K_j^T into S buffer j & 1
+                    const int s = j & 1;
+                    const uint32_t ph = (j >> 1) & 1u;
+                    if (!w.wait(kfull(s), ph, kDevErrMmaFull) ||
+                        !w.wait(sempty(s), ph ^ 1u, kDevErrMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after();
+                    const uint32_t q_s = sb + Cfg::OFF_Q;
+                    const uint32_t k_s = sb + Cfg::OFF_K + s * Cfg::KV_BYTES;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = (k >> 2) * Cfg::CHUNK_BYTES + (k & 3) * 32;
+                        mma_f16_ss(tmem_base + Cfg::T_S + s * 128, smem_desc_sw128(q_s + off, 16, 1024),
+                                   smem_desc_sw128(k_s + off, 16, 1024), Cfg::IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(kempty(s));
+                    mma_commit(sfull(s));
+                }
+                if (j >= 1) {
+                    // PV_{j-1} = P_{j-1} V_{j-1} into PV buffer (j-1) & 1
+                    const int t = j - 1, s = t & 1;
+                    const uint32_t ph = (t >> 1) & 1u;
+                    if (!w.wait(pfull(s), ph, kDevErrMmaFull) || !w.wait(vfull(s), ph, kDevErrMmaFull) ||
+                        !w.wait(pvempty(s), ph ^ 1u, kDevErrMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after();
+                    const uint32_t p_s = sb + Cfg::OFF_P + s * Cfg::P_BYTES;
+                    const uint32_t v_s = sb + Cfg::OFF_V + s * Cfg::KV_BYTES;
+#pragma unroll
+                    for (int k = 0; k < Cfg::BKV / 16; ++k) {
+                        // P: K-major, keys contiguous; V: MN-major, 64-column chunks 16 KB apart,
+                        // 16 key rows = 2048 bytes per k step
+                        const uint64_t ad =
+                            smem_desc_sw128(p_s + (k >> 2) * Cfg::CHUNK_BYTES + (k & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(v_s + k * 2048, Cfg::CHUNK_BYTES, 1024);
+                        mma_f16_ss(tmem_base + Cfg::T_PV + s * D, ad, bd, Cfg::IDESC_PV, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(vempty(s));
+                    mma_commit(pvfull(s));
+                }
+            }
+            mma_commit(drain);
+            w.drain(drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + output (warps 2-5)
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;              // query row in the tile == TMEM lane
+        const int qi = q0 + r;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+        float o[D];
+#pragma unroll
+        for (int d = 0; d < D; ++d) o[d] = 0.0f;
+        float m = -INFINITY, l = 0.0f, a_prev = 1.0f;
+        bool ok = true;
+
+        auto merge_pv = [&](int t) -> bool {          // O = a_prev * O + PV_t
+            const int s = t & 1;
+            const bool got = w.wait(pvfull(s), (t >> 1) & 1u, kDevErrEpilogueFull);
+            if (!named_bar_and(1, 128, got)) return false;
+            tcgen05_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(lane_base + Cfg::T_PV + s * D + c * 32, rr);
+                tmem_ld_wait(rr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c * 32 + i] = o[c * 32 + i] * a_prev + __uint_as_float(rr[i]);
+            }
+            tcgen05_fence_before();
+            mbar_arrive(pvempty(s));
+            return true;
+        };
+
+        for (int j = 0; j < nkv; ++j) {
+            const int s = j & 1;
+            const bool got = w.wait(sfull(s), (j >> 1) & 1u, kDevErrEpilogueFull);
+            if (!named_bar_and(1, 128, got)) {
+                ok = false;
+                break;
+            }
+            tcgen05_fence_after();
+            const uint32_t s_col = lane_base + Cfg::T_S + s * 128;
+            const int k0 = j * Cfg::BKV;
+            const int k_lim = p.causal ? min(p.Skv, qi + p.causal_offset + 1) : p.Skv;   // keys < k_lim
+            // pass 1: row maximum of the scaled, masked scores (log2 units)
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(s_col + c * 32, rr);
+                tmem_ld_wait(rr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float x = __uint_as_float(rr[i]) * p.scale_log2;
+                    if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, x);
+                }
+            }
+            const float m_new = fmaxf(m, mt);
+            const float alpha = (m_new == -INFINITY) ? 1.0f : exp2f(m - m_new);
+            // pass 2: P = exp2(x - m_new) in fp16 into shared memory, row sum in fp32
+            uint8_t* prow = smem + Cfg::OFF_P + s * Cfg::P_BYTES + r * 128;
+            float lsum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(s_col + c * 32, rr);
+                tmem_ld_wait(rr);
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int kk = k0 + c * 32 + 2 * i;
+                    const float x0 = __uint_as_float(rr[2 * i]) * p.scale_log2;
+                    const float x1 = __uint_as_float(rr[2 * i + 1]) * p.scale_log2;
+                    const float p0 = (kk < k_lim && m_new != -INFINITY) ? exp2f(x0 - m_new) : 0.0f;
+                    const float p1 = (kk + 1 < k_lim && m_new != -INFINITY) ? exp2f(x1 - m_new) : 0.0f;
+                    lsum += p0 + p1;
+                    __half2 h = __floats2half2_rn(p0, p1);
+                    packed[i] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                // keys c*32 .. c*32+31: chunk c/2, 16-byte pieces (c&1)*4 .. +3, swizzled by row
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int piece = (c & 1) * 4 + t;
+                    uint4 v;
+                    v.x = packed[4 * t];
+                    v.y = packed[4 * t + 1];
+                    v.z = packed[4 * t + 2];
+                    v.w = packed[4 * t + 3];
+                    *reinterpret_cast<uint4*>(prow + (c >> 1) * Cfg::CHUNK_BYTES + ((piece ^ (r & 7)) << 4)) = v;
+                }
+            }
+            tcgen05_fence_before();
+            mbar_arrive(sempty(s));          // S buffer free for S_{j+2}
+            fence_proxy_async_smem();
+            mbar_arrive(pfull(s));           // P_j ready for the MMA
+            l = l * alpha + lsum;
+            m = m_new;
+            if (j >= 1 && !merge_pv(j - 1)) {
+                ok = false;
+                break;
+            }
+            a_prev = alpha;
+        }
+        if (ok && nkv > 0) ok = merge_pv(nkv - 1);
+        // epilogue: O / l in fp16, and log-sum-exp
+        if (ok && qi < p.Sq) {
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            uint4* dst = reinterpret_cast<uint4*>(p.O + ((size_t)bh * p.Sq + qi) * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                uint32_t h[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    __half2 v = __floats2half2_rn(o[8 * c + 2 * i] * inv, o[8 * c + 2 * i + 1] * inv);
+                    h[i] = *reinterpret_cast<uint32_t*>(&v);
+                }
+                dst[c] = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+            if (p.lse)
+                p.lse[(size_t)bh * p.Sq + qi] = l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+
+    tcgen05_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tcgen05_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// O = 0 and lse = -inf for every row (no keys at all).
+__global__ void gsr_attention_empty_kernel(__half* O, float* lse, long long rows, int D) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < rows * D) O[i] = __float2half_rn(0.0f);
+    if (lse && i < rows) lse[i] = -INFINITY;
+}
+
+template <class Cfg>
+cudaError_t launch_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const AttnParams& p, cudaStream_t stream) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(gsr_attention_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const long long blocks = (long long)((p.Sq + Cfg::BQ - 1) / Cfg::BQ) * p.BH;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    gsr_attention_kernel<Cfg><<<(unsigned)blocks, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnParams& p, int D, cudaStream_t stream) {
+    if (D == 64) return launch_cfg<AttnCfg<64>>(tmQ, tmK, tmV, p, stream);
+    if (D == 128) return launch_cfg<AttnCfg<128>>(tmQ, tmK, tmV, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention_empty(__half* O, float* lse, long long rows, int D, cudaStream_t stream) {
+    const long long n = rows * D > rows ? rows * D : rows;
+    const long long blocks = (n + 255) / 256;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    gsr_attention_empty_kernel<<<(unsigned)blocks, 256, 0, stream>>>(O, lse, rows, D);
+    return cudaGetLastError();
+}
+
+}  // namespace gsr

@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -106,6 +107,29 @@ gsr_status encode_fp16_chunked(CUtensorMap* map, const void* base, uint64_t rows
         return GSR_ERR_CUDA;
     }
     return GSR_OK;
+}
+
+// (batch*heads, seq, D) fp16 as a 3-D tensor map {D, seq, BH}, box {64, 128, 1}: tiles never
+// cross heads and rows past `seq` are zero-filled.
+gsr_status encode_fp16_bsd(CUtensorMap* map, const void* base, uint64_t bh, uint64_t seq, uint64_t d) {
+    cuuint64_t dims[3] = {d, seq, bh};
+    cuuint64_t strides[2] = {d * 2, seq * d * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return GSR_ERR_CUDA;
+    }
+    return GSR_OK;
+}
+
+bool overlaps(const void* a, uint64_t an, const void* b, uint64_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a && b && an && bn && a0 < b0 + bn && b0 < a0 + an;
 }
 
 // Checks that need no GPU: sizes, null pointers, alignment, aliasing.  `*nothing` is set
@@ -468,6 +492,64 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
     p.epi = gsr::kEpiScaleRelu;
     p.bias = nullptr;
     e = gsr::launch_skinny_noalloc(tmBt, tmAt, p, mp, st);
+    return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+}
+
+gsr_status flash_attention_fwd(const void* Q, const void* K, const void* V, void* O, float* lse,
+                               int64_t batch, int64_t heads, int64_t seq_q, int64_t seq_kv,
+                               int64_t head_dim, float softmax_scale, int causal,
+                               CUstream_st* stream) {
+    if (batch < 0 || heads < 0 || seq_q < 0 || seq_kv < 0) return GSR_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return GSR_ERR_INVALID_ARG;
+    if (batch > INT_MAX || heads > INT_MAX || seq_q > INT_MAX || seq_kv > INT_MAX ||
+        batch * heads > INT_MAX)
+        return GSR_ERR_INVALID_ARG;
+    const int64_t BH = batch * heads;
+    if (BH == 0 || seq_q == 0) return GSR_OK;
+    if (!O || (seq_kv > 0 && (!Q || !K || !V)) || (seq_kv == 0 && !Q)) return GSR_ERR_INVALID_ARG;
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(O) || (Q && misaligned(Q)) || (K && misaligned(K)) || (V && misaligned(V)) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return GSR_ERR_ALIGNMENT;
+    const uint64_t q_bytes = (uint64_t)BH * seq_q * head_dim * 2;
+    const uint64_t kv_bytes = (uint64_t)BH * seq_kv * head_dim * 2;
+    const uint64_t lse_bytes = lse ? (uint64_t)BH * seq_q * 4 : 0;
+    if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
+        overlaps(O, q_bytes, V, kv_bytes) || overlaps(lse, lse_bytes, O, q_bytes) ||
+        overlaps(lse, lse_bytes, Q, q_bytes) || overlaps(lse, lse_bytes, K, kv_bytes) ||
+        overlaps(lse, lse_bytes, V, kv_bytes))
+        return GSR_ERR_ALIAS;
+    int dev = 0;
+    DeviceInfo info;
+    gsr_status s;
+    if ((s = device_info(&dev, &info)) != GSR_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (seq_kv == 0) {   // no keys at all: every row is empty
+        e = gsr::launch_attention_empty(static_cast<__half*>(O), lse, BH * seq_q, (int)head_dim, st);
+        return e == cudaSuccess ? GSR_OK : cuda_fail(e);
+    }
+    StreamState ss;
+    if ((s = stream_state(dev, st, 0, 0, &ss)) != GSR_OK) return s;
+    if ((s = load_encoder()) != GSR_OK) return s;
+    CUtensorMap tmQ, tmK, tmV;
+    if ((s = encode_fp16_bsd(&tmQ, Q, BH, seq_q, head_dim)) != GSR_OK) return s;
+    if ((s = encode_fp16_bsd(&tmK, K, BH, seq_kv, head_dim)) != GSR_OK) return s;
+    if ((s = encode_fp16_bsd(&tmV, V, BH, seq_kv, head_dim)) != GSR_OK) return s;
+    const double scale = softmax_scale != 0.0f ? (double)softmax_scale : 1.0 / std::sqrt((double)head_dim);
+    gsr::AttnParams p;
+    p.BH = (int)BH;
+    p.Sq = (int)seq_q;
+    p.Skv = (int)seq_kv;
+    p.causal = causal ? 1 : 0;
+    p.causal_offset = (int)(seq_kv - seq_q);
+    p.scale_log2 = (float)(scale * 1.4426950408889634);
+    p.O = static_cast<__half*>(O);
+    p.lse = lse;
+    p.err = ss.err;
+    p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    p.test_flags = g_test_flags.load(std::memory_order_relaxed);
+    e = gsr::launch_attention(tmQ, tmK, tmV, p, (int)head_dim, st);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }
 

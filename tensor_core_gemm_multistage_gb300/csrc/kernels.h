@@ -20,6 +20,7 @@ enum DeviceError : int {
     kDevErrTeardown = 5,        // teardown: in-flight copies or MMAs did not drain
     kDevErrKernelTiled = 0x100,
     kDevErrKernelSkinny = 0x200,
+    kDevErrKernelAttention = 0x300,
 };
 
 // Test-only flags (gsr_set_test_flags).
@@ -74,6 +75,25 @@ inline void skinny_split(int n_tiles, int k_blocks, int sms, int* slabs, int* ct
     *slabs = S;
     *ctas = (int)(items < sms ? items : sms);
 }
+
+struct AttnParams {
+    int BH;                 // batch * heads
+    int Sq, Skv;
+    int causal;             // keep key k for query q when k <= q + causal_offset
+    int causal_offset;      // Skv - Sq
+    float scale_log2;       // softmax scale * log2(e)
+    __half* O;              // (BH, Sq, D) row-major
+    float* lse;             // optional (BH, Sq): natural-log log-sum-exp of the scaled scores
+    int* err;
+    uint64_t timeout_ns;
+    uint32_t test_flags;
+};
+
+// Attention forward: Q, K, V as 3-D tensor maps {D, seq, BH} with 64 x 128 x 1 boxes.
+cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnParams& p, int D, cudaStream_t stream);
+// O = 0, lse = -inf for `rows` rows of width D (no keys).
+cudaError_t launch_attention_empty(__half* O, float* lse, long long rows, int D, cudaStream_t stream);
 
 // Tiled path: persistent, one 128 x BN output tile per CTA iteration.
 // bn is 128 or 256.  grid = min(num_tiles, num_sms).

@@ -1,0 +1,121 @@
+"""GPU parity of flash_attention_fwd against the fp64 attention oracle.
+
+Acceptance: per element |gpu - oracle| <= 1e-2 + 1e-2 |oracle| (the operator tests' bound),
+relative Frobenius error <= 2e-3 (P is rounded to fp16 before the second product: about
+2^-12 relative per probability, averaged over the keys), log-sum-exp within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tensor_core_gemm_multistage_gb300 as gsr
+from oracle.attention import attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gsr.build()
+    yield
+
+
+def inputs(B, H, Sq, Skv, D, seed, same_keys=False):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, Sq, D, generator=g).half()
+    k = torch.randn(B, H, Skv, D, generator=g).half()
+    if same_keys:
+        k = k[:, :, :1].expand(B, H, Skv, D).contiguous()
+    v = torch.randn(B, H, Skv, D, generator=g).half()
+    return q, k, v
+
+
+def run(q, k, v, causal=False, scale=0.0):
+    dev = torch.device("cuda", 0)
+    B, H, Sq, D = q.shape
+    O = torch.full((B, H, Sq, D), float("nan"), dtype=torch.float16, device=dev)
+    lse = torch.full((B, H, Sq), float("nan"), dtype=torch.float32, device=dev)
+    gsr.flash_attention_fwd(q.to(dev), k.to(dev), v.to(dev), O, lse, softmax_scale=scale, causal=causal)
+    status, code = gsr.device_status()
+    assert status == gsr.Status.OK, hex(code)
+    return O.cpu().numpy(), lse.cpu().numpy()
+
+
+def check(q, k, v, causal=False, scale=0.0):
+    o, lse = run(q, k, v, causal, scale)
+    ref, ref_lse, _ = attention(q, k, v, scale=None if scale == 0.0 else scale, causal=causal,
+                                return_lse=True)
+    x = o.astype(np.float64)
+    y = ref.astype(np.float64)
+    assert not np.isnan(x).any(), "unwritten outputs"
+    err = np.abs(x - y)
+    assert np.all(err <= 1e-2 + 1e-2 * np.abs(y)), "worst %g" % err.max()
+    ny = np.linalg.norm(y)
+    if ny > 0:
+        assert np.linalg.norm(x - y) / ny <= 2e-3, np.linalg.norm(x - y) / ny
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.all(np.abs(lse[fin] - ref_lse[fin]) <= 1e-3)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,S,D", [(1, 1, 128, 64), (1, 2, 256, 128), (2, 3, 200, 64),
+                                     (1, 2, 333, 128), (1, 1, 1024, 128)])
+def test_self_attention(B, H, S, D, causal):
+    check(*inputs(B, H, S, S, D, seed=S + D), causal=causal)
+
+
+@pytest.mark.parametrize("Sq,Skv", [(100, 333), (1, 515), (256, 64), (64, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_cross_lengths(Sq, Skv, causal):
+    check(*inputs(1, 2, Sq, Skv, 128, seed=Sq * 7 + Skv), causal=causal)
+
+
+def test_explicit_scale_and_identical_keys():
+    q, k, v = inputs(1, 2, 130, 257, 64, seed=3, same_keys=True)
+    check(q, k, v, scale=0.3)
+    o, _ = run(q, k, v, scale=0.3)
+    mean = v.double().mean(dim=2, keepdim=True).numpy()
+    assert np.allclose(o.astype(np.float64), np.broadcast_to(mean, o.shape), atol=2e-3)
+
+
+def test_no_keys_and_fully_masked_rows():
+    q, k, v = inputs(1, 1, 200, 70, 64, seed=4)
+    check(q, k, v, causal=True)                    # rows 0..129 have no key
+    o, lse = run(q, k, v, causal=True)
+    assert np.all(o[0, 0, :130] == 0) and np.all(np.isneginf(lse[0, 0, :130]))
+    dev = torch.device("cuda", 0)
+    O = torch.full((1, 1, 5, 64), float("nan"), dtype=torch.float16, device=dev)
+    lse0 = torch.zeros(1, 1, 5, dtype=torch.float32, device=dev)
+    empty = torch.empty(1, 1, 0, 64, dtype=torch.float16, device=dev)
+    gsr.flash_attention_fwd(q[:, :, :5].to(dev).contiguous(), empty, empty, O, lse0)
+    torch.cuda.synchronize()
+    assert torch.all(O == 0) and torch.all(torch.isinf(lse0))
+
+
+def test_timeout_reports_and_recovers():
+    q, k, v = inputs(1, 1, 256, 256, 64, seed=5)
+    gsr.set_wait_timeout_ns(50_000_000)
+    gsr.set_test_flags(1)
+    try:
+        dev = torch.device("cuda", 0)
+        O = torch.zeros(1, 1, 256, 64, dtype=torch.float16, device=dev)
+        gsr.flash_attention_fwd(q.to(dev), k.to(dev), v.to(dev), O)
+        status, code = gsr.device_status()
+    finally:
+        gsr.set_test_flags(0)
+        gsr.set_wait_timeout_ns(1_000_000_000)
+    assert status == gsr.Status.ERR_DEVICE_TIMEOUT and code & 0xF00 == 0x300
+    check(q, k, v)
+
+
+def test_validation():
+    dev = torch.device("cuda", 0)
+    t = torch.empty(1, 1, 128, 64, dtype=torch.float16, device=dev)
+    L = gsr.lib()
+    import ctypes
+    vp = ctypes.c_void_p
+    args = lambda o, d: (vp(t.data_ptr()), vp(t.data_ptr()), vp(t.data_ptr()), vp(o), None, 1, 1, 128,
+                         128, d, ctypes.c_float(0.0), 0, None)
+    assert L.flash_attention_fwd(*args(t.data_ptr(), 96)) == gsr.Status.ERR_INVALID_ARG
+    assert L.flash_attention_fwd(*args(t.data_ptr(), 64)) == gsr.Status.ERR_ALIAS
