@@ -36,7 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from tensor_core_gemm_multistage_gb300.workloads import WORKLOADS, workload_inputs  # noqa: E402
+from tensor_core_gemm_multistage_gb300.workloads import (ATTN_WORKLOADS, WORKLOADS,  # noqa: E402
+                                                          workload_inputs)
 
 METRIC = "fused GEMM+scale+ReLU TFLOP/s and % of GB300 dense FP16 peak, 1 GPU"
 DEFAULT_WORKLOAD = "square8192"
@@ -430,13 +431,110 @@ def run_gsr(args, w):
     return 0
 
 
+def run_attention(args, w):
+    """Attention forward on one GPU: same timing rules as the GEMM arm."""
+    import torch
+
+    import tensor_core_gemm_multistage_gb300 as gsr
+    from tensor_core_gemm_multistage_gb300.workloads import attention_inputs
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gsr.build()
+    q, k, v = attention_inputs(w, seed=0, device=dev)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gsr.flash_attention_fwd(q, k, v, o, causal=w.causal, stream=stream)
+
+    sampler = ClockSampler(gpu_uuid()).start() if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    status, code = gsr.device_status(stream)
+    if status != gsr.Status.OK:
+        raise RuntimeError("device status %s code %#x" % (status.name, code))
+    kernel_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world)
+    context = None
+    if args.torch_context:
+        sdpa = lambda: torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=w.causal)
+        for _ in range(args.warmup):
+            sdpa()
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.steps):
+            sdpa()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        ms = c0.elapsed_time(c1) / args.steps
+        context = {"torch_sdpa": {"ms_per_step": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12}}
+    if sampler is not None:
+        sampler.stop()
+    if rank != 0:
+        return 0
+    peaks, peaks_src = measured_peaks()
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": "attention forward TFLOP/s (FlashAttention-style, fp16 in, fp32 softmax), 1 GPU",
+        "value": whole_job_tflops(world, w.flops, kernel_ms), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded randn, fp16)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
+                   "flops": "4*B*H*D*(unmasked query-key pairs)",
+                   "l2": "inputs %d MiB; no flush" % (3 * w.B * w.H * w.S * w.D * 2 >> 20)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "kernel": "gsr_attention_kernel", "traffic": None,
+                     "peak_source": "%s: bf16_tflops burst; fp16 rate taken equal" % peaks_src},
+        "gpu_launches": args.steps,
+    }
+    if sampler is not None:
+        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+    if context is not None:
+        line["context"] = context
+    if world == 1 and args.cpu_seconds > 0:
+        from oracle.attention import attention
+        qs, ks, vs = (x[:1, :1].cpu() for x in (q, k, v))      # one head
+        t = time.perf_counter()
+        attention(qs, ks, vs, causal=w.causal)
+        secs = time.perf_counter() - t
+        line["cpu_baseline"] = {"value": 4 * w.D * w.pairs / secs / 1e12, "unit": "TFLOP/s",
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": "one (batch, head) of the workload, %.1f s" % secs}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gsr", "reference"], default="gsr")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(ATTN_WORKLOADS),
+                    default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--epilogue", choices=["scale_relu", "scale", "bias_gelu"], default="scale_relu",
@@ -447,6 +545,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.workload in ATTN_WORKLOADS:
+        if args.impl == "reference":
+            ap.error("the reference arm times the GEMM oracle; attention workloads are gsr-only")
+        return run_attention(args, ATTN_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t s_col = lane_base + Cfg::T_S + s * 128;
             const int k0 = j * Cfg::BKV;
             const int k_lim = p.causal ? min(p.Skv, qi + p.causal_offset + 1) : p.Skv;   // keys < k_lim
+            const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
             // pass 1: row maximum of the scaled, masked scores (log2 units)
             float mt = -INFINITY;
 #pragma unroll
@@ -268,15 +269,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 uint32_t rr[32];
                 tmem_ld_32x32b_x32(s_col + c * 32, rr);
                 tmem_ld_wait(rr);
+                if (!masked) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = __uint_as_float(rr[i]) * p.scale_log2;
-                    if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, x);
+                    for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(rr[i]) * p.scale_log2);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * p.scale_log2);
                 }
             }
             const float m_new = fmaxf(m, mt);
-            const float alpha = (m_new == -INFINITY) ? 1.0f : exp2f(m - m_new);
-            // pass 2: P = exp2(x - m_new) in fp16 into shared memory, row sum in fp32
+            const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
+            const float neg_m = (m_new == -INFINITY) ? 0.0f : -m_new;
+            // pass 2: P = 2^(x - m_new) in fp16 into shared memory, row sum in fp32
             uint8_t* prow = smem + Cfg::OFF_P + s * Cfg::P_BYTES + r * 128;
             float lsum = 0.0f;
 #pragma unroll
@@ -287,11 +292,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 uint32_t packed[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int kk = k0 + c * 32 + 2 * i;
-                    const float x0 = __uint_as_float(rr[2 * i]) * p.scale_log2;
-                    const float x1 = __uint_as_float(rr[2 * i + 1]) * p.scale_log2;
-                    const float p0 = (kk < k_lim && m_new != -INFINITY) ? exp2f(x0 - m_new) : 0.0f;
-                    const float p1 = (kk + 1 < k_lim && m_new != -INFINITY) ? exp2f(x1 - m_new) : 0.0f;
+                    float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), p.scale_log2, neg_m));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), p.scale_log2, neg_m));
+                    if (masked) {
+                        const int kk = k0 + c * 32 + 2 * i;
+                        if (kk >= k_lim || m_new == -INFINITY) p0 = 0.0f;
+                        if (kk + 1 >= k_lim || m_new == -INFINITY) p1 = 0.0f;
+                    }
                     lsum += p0 + p1;
                     __half2 h = __floats2half2_rn(p0, p1);
                     packed[i] = *reinterpret_cast<uint32_t*>(&h);

@@ -274,6 +274,13 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_maj
            ((uint32_t)(M >> 4) << 24);
 }
 
+// 2^x with the special-function unit (ex2.approx.ftz: about 2 ulp; -inf gives +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------------------
 // Epilogue arithmetic: y = max(alpha * acc, 0), rounded to fp16 (nearest even)
 // ---------------------------------------------------------------------------

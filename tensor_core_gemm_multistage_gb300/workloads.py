@@ -86,3 +86,42 @@ def make_bias(N: int, seed: int = 0):
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     return (torch.randn(N, generator=g, dtype=torch.float32) * 2).half().contiguous()
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Attention forward: Q (B,H,S,D), K/V (B,H,S,D), fp16, randn inputs."""
+    name: str
+    B: int
+    H: int
+    S: int
+    D: int
+    causal: bool
+
+    @property
+    def pairs(self) -> int:
+        """(query, key) pairs that are not masked, per head."""
+        return self.S * (self.S + 1) // 2 if self.causal else self.S * self.S
+
+    @property
+    def flops(self) -> int:
+        """Q K^T and P V: 2 x 2 D flops per unmasked (query, key) pair."""
+        return 4 * self.B * self.H * self.D * self.pairs
+
+
+ATTN_WORKLOADS = {
+    w.name: w for w in (
+        AttnWorkload("attn_b4_h32_s4096_d128", 4, 32, 4096, 128, False),
+        AttnWorkload("attn_b4_h32_s4096_d128_causal", 4, 32, 4096, 128, True),
+        AttnWorkload("attn_b8_h16_s2048_d64", 8, 16, 2048, 64, False),
+    )
+}
+
+
+def attention_inputs(w: AttnWorkload, seed: int = 0, device="cpu"):
+    """Q, K, V float16 from randn (drawn on ``device`` with a seeded generator)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    shape = (w.B, w.H, w.S, w.D)
+    return tuple(torch.randn(shape, generator=g, device=device, dtype=torch.float32).half()
+                 for _ in range(3))
