@@ -7,9 +7,12 @@
 // matrix products.  Its thread roles follow "TileLang异步协作终极指南" (producers load K/V, one
 // role computes QK^T, another the softmax and the output), rebuilt on tcgen05:
 //
-//  * one CTA per (128-query tile, batch x head); 192 threads: warp 0 issues TMA copies (Q
+//  * one CTA per (128-query tile, batch x head); 320 threads: warp 0 issues TMA copies (Q
 //    once, then K_j and V_j into a 2-stage ring), warp 1 issues every MMA from one lane,
-//    warps 2-5 run the softmax, one query row per thread (TMEM lane = row);
+//    warps 2-9 run the softmax in two groups of four warps: each query row (TMEM lane) has
+//    one thread in each group; both take the row maximum over all 128 keys of a tile, each
+//    exponentiates half of the keys and accumulates half of the output columns, and the two
+//    halves of the row sum are added once at the end;
 //  * S_j = Q K_j^T (M 128 queries, N 128 keys, K = head_dim) accumulates in TMEM, two
 //    buffers, so S_{j+1} is computed while the softmax reads S_j;
 //  * the softmax reads its S row twice from TMEM (max, then exponentials), writes P_j in
@@ -36,14 +39,19 @@ struct AttnCfg {
     static constexpr int Q_BYTES = BQ * D * 2;
     static constexpr int KV_BYTES = BKV * D * 2;
     static constexpr int P_BYTES = BQ * BKV * 2;      // 32 KB: two 64-key chunks
-    static constexpr int NUM_THREADS = 192;
+    static constexpr int G = 2;                       // softmax warp groups per query row
+    static constexpr int SM_THREADS = 128 * G;        // softmax threads
+    static constexpr int NUM_THREADS = 64 + SM_THREADS;
+    static constexpr int KEYS_PER_G = BKV / G;        // keys of a row each group exponentiates
+    static constexpr int DCOLS_PER_G = D / G;         // output columns each group accumulates
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
     static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
     static constexpr int NUM_BARS = 1 + 9 * 2 + 1;
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_LSUM = OFF_BAR + NUM_BARS * 8;   // (G-1) x 128 partial row sums
+    static constexpr int OFF_MISC = OFF_LSUM + (G - 1) * BQ * 4;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_COLS = 512;             // S 2 x 128, PV 2 x D
     static constexpr uint32_t T_S = 0, T_PV = 256;
@@ -51,6 +59,7 @@ struct AttnCfg {
     static constexpr uint32_t IDESC_PV = idesc_f16_f32(BQ, D, false, true);     // P K-major, V MN-major
 
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(G == 1 || G == 2, "one or two softmax groups");
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
     static_assert(T_PV + 2 * D <= TMEM_COLS, "TMEM budget");
 };
@@ -100,10 +109,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             mbar_init(vfull(s), 1);
             mbar_init(vempty(s), 1);
             mbar_init(sfull(s), 1);
-            mbar_init(sempty(s), 128);
-            mbar_init(pfull(s), 128);
+            mbar_init(sempty(s), Cfg::SM_THREADS);
+            mbar_init(pfull(s), Cfg::SM_THREADS);
             mbar_init(pvfull(s), 1);
-            mbar_init(pvempty(s), 128);
+            mbar_init(pvempty(s), Cfg::SM_THREADS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0u;
@@ -221,29 +230,34 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax + output (warps 2-5)
+        // ------------------------------------------------------------ softmax + output (warps 2-9)
+        constexpr int G = Cfg::G;
+        constexpr int KG = Cfg::KEYS_PER_G;
+        constexpr int DG = Cfg::DCOLS_PER_G;
         const int quad = warp & 3;
+        const int g = (warp - 2) >> 2;               // softmax group
         const int r = quad * 32 + lane;              // query row in the tile == TMEM lane
         const int qi = q0 + r;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-        float o[D];
+        const bool scale_pos = p.scale_log2 >= 0.0f;
+        float o[DG];
 #pragma unroll
-        for (int d = 0; d < D; ++d) o[d] = 0.0f;
+        for (int d = 0; d < DG; ++d) o[d] = 0.0f;
         float m = -INFINITY, l = 0.0f, a_prev = 1.0f;
         bool ok = true;
 
-        auto merge_pv = [&](int t) -> bool {          // O = a_prev * O + PV_t
+        auto merge_pv = [&](int t) -> bool {          // O (this group's columns) = a_prev O + PV_t
             const int s = t & 1;
             const bool got = w.wait(pvfull(s), (t >> 1) & 1u, kDevErrEpilogueFull);
-            if (!named_bar_and(1, 128, got)) return false;
+            if (!named_bar_and(1, Cfg::SM_THREADS, got)) return false;
             tcgen05_fence_after();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < DG / 32; ++c) {
                 uint32_t rr[32];
-                tmem_ld_32x32b_x32(lane_base + Cfg::T_PV + s * D + c * 32, rr);
+                tmem_ld_32x32b_x32(lane_base + Cfg::T_PV + s * D + g * DG + c * 32, rr);
                 tmem_ld_wait(rr);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[c * 32 + i] = o[c * 32 + i] * a_prev + __uint_as_float(rr[i]);
+                for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], a_prev, __uint_as_float(rr[i]));
             }
             tcgen05_fence_before();
             mbar_arrive(pvempty(s));
@@ -253,7 +267,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         for (int j = 0; j < nkv; ++j) {
             const int s = j & 1;
             const bool got = w.wait(sfull(s), (j >> 1) & 1u, kDevErrEpilogueFull);
-            if (!named_bar_and(1, 128, got)) {
+            if (!named_bar_and(1, Cfg::SM_THREADS, got)) {
                 ok = false;
                 break;
             }
@@ -262,8 +276,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int k0 = j * Cfg::BKV;
             const int k_lim = p.causal ? min(p.Skv, qi + p.causal_offset + 1) : p.Skv;   // keys < k_lim
             const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
-            // pass 1: row maximum of the scaled, masked scores (log2 units)
-            float mt = -INFINITY;
+            // pass 1 (whole row): maximum of the scaled, masked scores, in log2 units.
+            // `masked` differs between rows of one warp on a diagonal tile, so the TMEM loads
+            // (.sync.aligned: the whole warp together) stay outside the branch.
+            float mt = -INFINITY, hi = -INFINITY, lo = INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t rr[32];
@@ -271,23 +287,28 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 tmem_ld_wait(rr);
                 if (!masked) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(rr[i]) * p.scale_log2);
+                    for (int i = 0; i < 32; ++i) {
+                        hi = fmaxf(hi, __uint_as_float(rr[i]));
+                        lo = fminf(lo, __uint_as_float(rr[i]));
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * p.scale_log2);
                 }
             }
+            if (!masked) mt = (scale_pos ? hi : lo) * p.scale_log2;
             const float m_new = fmaxf(m, mt);
             const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
             const float neg_m = (m_new == -INFINITY) ? 0.0f : -m_new;
-            // pass 2: P = 2^(x - m_new) in fp16 into shared memory, row sum in fp32
+            // pass 2 (this group's keys): P = 2^(x - m_new) in fp16 into shared memory
             uint8_t* prow = smem + Cfg::OFF_P + s * Cfg::P_BYTES + r * 128;
             float lsum = 0.0f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < KG / 32; ++c) {
+                const int kc = g * KG + c * 32;          // first key of this 32-key slice
                 uint32_t rr[32];
-                tmem_ld_32x32b_x32(s_col + c * 32, rr);
+                tmem_ld_32x32b_x32(s_col + kc, rr);
                 tmem_ld_wait(rr);
                 uint32_t packed[16];
 #pragma unroll
@@ -295,7 +316,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), p.scale_log2, neg_m));
                     float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), p.scale_log2, neg_m));
                     if (masked) {
-                        const int kk = k0 + c * 32 + 2 * i;
+                        const int kk = k0 + kc + 2 * i;
                         if (kk >= k_lim || m_new == -INFINITY) p0 = 0.0f;
                         if (kk + 1 >= k_lim || m_new == -INFINITY) p1 = 0.0f;
                     }
@@ -303,23 +324,23 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     __half2 h = __floats2half2_rn(p0, p1);
                     packed[i] = *reinterpret_cast<uint32_t*>(&h);
                 }
-                // keys c*32 .. c*32+31: chunk c/2, 16-byte pieces (c&1)*4 .. +3, swizzled by row
+                // keys kc .. kc+31: 64-key chunk kc/64, 16-byte pieces ((kc%64)/8) .. +3, swizzled by row
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const int piece = (c & 1) * 4 + t;
+                    const int piece = ((kc & 63) >> 3) + t;
                     uint4 v;
                     v.x = packed[4 * t];
                     v.y = packed[4 * t + 1];
                     v.z = packed[4 * t + 2];
                     v.w = packed[4 * t + 3];
-                    *reinterpret_cast<uint4*>(prow + (c >> 1) * Cfg::CHUNK_BYTES + ((piece ^ (r & 7)) << 4)) = v;
+                    *reinterpret_cast<uint4*>(prow + (kc >> 6) * Cfg::CHUNK_BYTES + ((piece ^ (r & 7)) << 4)) = v;
                 }
             }
             tcgen05_fence_before();
             mbar_arrive(sempty(s));          // S buffer free for S_{j+2}
             fence_proxy_async_smem();
             mbar_arrive(pfull(s));           // P_j ready for the MMA
-            l = l * alpha + lsum;
+            l = l * alpha + lsum;            // this group's part of the row sum
             m = m_new;
             if (j >= 1 && !merge_pv(j - 1)) {
                 ok = false;
@@ -328,12 +349,26 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             a_prev = alpha;
         }
         if (ok && nkv > 0) ok = merge_pv(nkv - 1);
-        // epilogue: O / l in fp16, and log-sum-exp
+        // the row sum: group 0 adds the other groups' parts (one exchange per kernel)
+        float* lpart = reinterpret_cast<float*>(smem + Cfg::OFF_LSUM);
+        if (G > 1) {
+            if (g > 0) lpart[(g - 1) * Cfg::BQ + r] = l;
+            named_bar_sync(2, Cfg::SM_THREADS);
+            if (g == 0) {
+                float total = l;
+#pragma unroll
+                for (int gg = 1; gg < G; ++gg) total += lpart[(gg - 1) * Cfg::BQ + r];
+                lpart[r] = total;                // publish the full sum back
+            }
+            named_bar_sync(2, Cfg::SM_THREADS);
+            l = lpart[r];
+        }
+        // epilogue: this group's output columns, O / l in fp16, and the log-sum-exp
         if (ok && qi < p.Sq) {
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            uint4* dst = reinterpret_cast<uint4*>(p.O + ((size_t)bh * p.Sq + qi) * D);
+            uint4* dst = reinterpret_cast<uint4*>(p.O + ((size_t)bh * p.Sq + qi) * D + g * DG);
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
+            for (int c = 0; c < DG / 8; ++c) {
                 uint32_t h[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -342,7 +377,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
                 dst[c] = make_uint4(h[0], h[1], h[2], h[3]);
             }
-            if (p.lse)
+            if (p.lse && g == 0)
                 p.lse[(size_t)bh * p.Sq + qi] = l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
     }
