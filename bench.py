@@ -42,18 +42,24 @@ from tensor_core_gemm_multistage_gb300.workloads import (ATTN_WORKLOADS, WORKLOA
 METRIC = "fused GEMM+scale+ReLU TFLOP/s and % of GB300 dense FP16 peak, 1 GPU"
 DEFAULT_WORKLOAD = "square8192"
 L2_BYTES = 126 * 1024 * 1024
-KERNEL_SOURCES = ["csrc/gemm_tiled.cu", "csrc/gemm_pair.cu", "csrc/gemm_skinny.cu",
-                  "csrc/ptx.cuh", "csrc/device_common.cuh", "csrc/kernels.h"]
+# The sources each kernel is built from: a DRAM-traffic figure stays valid while they do.
+_SHARED_SOURCES = ["csrc/ptx.cuh", "csrc/device_common.cuh", "csrc/kernels.h"]
+KERNEL_SOURCES = {
+    "gsr_tiled_kernel": ["csrc/gemm_tiled.cu"] + _SHARED_SOURCES,
+    "gsr_pair_kernel": ["csrc/gemm_pair.cu"] + _SHARED_SOURCES,
+    "gsr_skinny_kernel": ["csrc/gemm_skinny.cu"] + _SHARED_SOURCES,
+    "gsr_attention_kernel": ["csrc/attention_fwd.cu"] + _SHARED_SOURCES,
+}
 KERNEL_NAMES = {0: "gsr_tiled_kernel", 1: "gsr_skinny_kernel", 2: "gsr_pair_kernel"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 # ---------------------------------------------------------------------------- helpers
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "tensor_core_gemm_multistage_gb300")
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(pkg, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -64,7 +70,7 @@ def read_traffic(workload: str, kernel: str):
     kernel sources; lines: `workload kernel sources_hash bytes_per_launch note...`."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    cur = kernel_source_hash()
+    cur = kernel_source_hash(kernel)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = line.split()
@@ -452,39 +458,44 @@ def run_attention(args, w):
     def step():
         gsr.flash_attention_fwd(q, k, v, o, causal=w.causal, stream=stream)
 
+    # Q, K, V and O that fit in L2 are evicted between steps (a 256 MiB write outside each
+    # step's event pair), so every step reads its inputs from HBM.
+    io_bytes = 4 * w.B * w.H * w.S * w.D * 2
+    flush = (torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+             if io_bytes <= 2 * L2_BYTES else None)
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
     sampler = ClockSampler(gpu_uuid()).start() if rank == 0 else None
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     barrier(world)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     t_wall0 = time.time()
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    kernel_ms = timed(step)
     t_wall1 = time.time()
     barrier(world)
     status, code = gsr.device_status(stream)
     if status != gsr.Status.OK:
         raise RuntimeError("device status %s code %#x" % (status.name, code))
-    kernel_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world)
+    kernel_ms = max_over_ranks(kernel_ms, world)
     context = None
     if args.torch_context:
         sdpa = lambda: torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=w.causal)
         for _ in range(args.warmup):
             sdpa()
         torch.cuda.synchronize()
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record(stream)
-        for _ in range(args.steps):
-            sdpa()
-        c1.record(stream)
-        torch.cuda.synchronize()
-        ms = c0.elapsed_time(c1) / args.steps
+        ms = timed(sdpa)
         context = {"torch_sdpa": {"ms_per_step": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12}}
     if sampler is not None:
         sampler.stop()
@@ -501,9 +512,11 @@ def run_attention(args, w):
         "data": "synthetic (seeded randn, fp16)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
                    "flops": "4*B*H*D*(unmasked query-key pairs)",
-                   "l2": "inputs %d MiB; no flush" % (3 * w.B * w.H * w.S * w.D * 2 >> 20)},
+                   "l2": ("Q, K, V, O %d MiB; " % (io_bytes >> 20)) +
+                         ("flush L2 between steps" if flush is not None else "larger than L2, no flush")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "kernel": "gsr_attention_kernel", "traffic": None,
+                     "frac": achieved / peak, "kernel": "gsr_attention_kernel",
+                     "traffic": read_traffic(w.name, "gsr_attention_kernel"),
                      "peak_source": "%s: bf16_tflops burst; fp16 rate taken equal" % peaks_src},
         "gpu_launches": args.steps,
     }

@@ -186,7 +186,9 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
  * device error code, 0 if none: low byte = which wait gave up (1 producer
  * waiting for a free stage, 2 MMA issuer waiting for loaded data, 3 MMA issuer
  * waiting for a free accumulator, 4 epilogue waiting for a finished
- * accumulator, 5 teardown drain), 0x100 = tiled kernel, 0x200 = small-M.
+ * accumulator, 5 teardown drain, 6 shared-memory window not 1024-byte aligned:
+ * the kernel returned at once), 0x100 = tiled kernel, 0x200 = small-M,
+ * 0x300 = attention.
  */
 gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
 

@@ -10,9 +10,11 @@
 //  * one CTA per (128-query tile, batch x head); 320 threads: warp 0 issues TMA copies (Q
 //    once, then K_j and V_j into a 2-stage ring), warp 1 issues every MMA from one lane,
 //    warps 2-9 run the softmax in two groups of four warps: each query row (TMEM lane) has
-//    one thread in each group; both take the row maximum over all 128 keys of a tile, each
-//    exponentiates half of the keys and accumulates half of the output columns, and the two
-//    halves of the row sum are added once at the end;
+//    one thread in each group, and each thread owns half of the row's keys and half of its
+//    output columns.  Per tile the two threads of a row exchange their partial maxima through
+//    shared memory (the block-wide vote that ends a failed wait doubles as that exchange),
+//    then each exponentiates its keys and merges its columns; the halves of the row sum are
+//    added once at the end;
 //  * S_j = Q K_j^T (M 128 queries, N 128 keys, K = head_dim) accumulates in TMEM, two
 //    buffers, so S_{j+1} is computed while the softmax reads S_j;
 //  * the softmax reads its S row twice from TMEM (max, then exponentials), writes P_j in
@@ -50,28 +52,58 @@ struct AttnCfg {
     static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
     static constexpr int NUM_BARS = 1 + 9 * 2 + 1;
-    static constexpr int OFF_LSUM = OFF_BAR + NUM_BARS * 8;   // (G-1) x 128 partial row sums
-    static constexpr int OFF_MISC = OFF_LSUM + (G - 1) * BQ * 4;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    // [2 S buffers][G][128] partial row maxima; after the last tile the slot of the unused
+    // buffer carries the partial row sums
+    static constexpr int OFF_MAXP = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_MISC = OFF_MAXP + 2 * G * BQ * 4;
+    // no alignment slack: the window is declared 1024-byte aligned and the kernel checks it
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TMEM_COLS = 512;             // S 2 x 128, PV 2 x D
     static constexpr uint32_t T_S = 0, T_PV = 256;
     static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q, K both K-major
     static constexpr uint32_t IDESC_PV = idesc_f16_f32(BQ, D, false, true);     // P K-major, V MN-major
 
+    static constexpr bool kExchangeMax = true;        // pass 1 over own keys + exchange
+    static constexpr bool kPacked = true;             // packed f32x2 arithmetic
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(G == 1 || G == 2, "one or two softmax groups");
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
     static_assert(T_PV + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
+// (y0, y1) = (a0 b0 + c0, a1 b1 + c1), packed into one instruction when P.
+template <bool P>
+__device__ __forceinline__ void fma_pair(float& y0, float& y1, float a0, float a1, float b0, float b1, float c0,
+                                         float c1) {
+    if constexpr (P) {
+        ffma2(y0, y1, a0, a1, b0, b1, c0, c1);
+    } else {
+        y0 = fmaf(a0, b0, c0);
+        y1 = fmaf(a1, b1, c1);
+    }
+}
+// (y0, y1) += (a0, a1)
+template <bool P>
+__device__ __forceinline__ void add_pair(float& y0, float& y1, float a0, float a1) {
+    if constexpr (P) {
+        fadd2(y0, y1, a0, a1);
+    } else {
+        y0 += a0;
+        y1 += a1;
+    }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gsr_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     constexpr int D = Cfg::D;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_s = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {                // the 128-byte-swizzled operands need it
+        if (threadIdx.x == 0) atomicCAS(p.err, 0, kDevErrKernelAttention | kDevErrLayout);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     const uint32_t sb = smem_u32(smem);
 
     // barriers: 0 qfull | 1+s kfull | 3+s kempty | 5+s vfull | 7+s vempty | 9+s sfull |
@@ -234,22 +266,28 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         constexpr int G = Cfg::G;
         constexpr int KG = Cfg::KEYS_PER_G;
         constexpr int DG = Cfg::DCOLS_PER_G;
+        constexpr bool XM = Cfg::kExchangeMax;
+        constexpr int P1_CHUNKS = XM ? KG / 32 : Cfg::BKV / 32;   // 32-key slices pass 1 reads
         const int quad = warp & 3;
         const int g = (warp - 2) >> 2;               // softmax group
         const int r = quad * 32 + lane;              // query row in the tile == TMEM lane
         const int qi = q0 + r;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
         const bool scale_pos = p.scale_log2 >= 0.0f;
+        const float sl2 = p.scale_log2;
         float o[DG];
 #pragma unroll
         for (int d = 0; d < DG; ++d) o[d] = 0.0f;
         float m = -INFINITY, l = 0.0f, a_prev = 1.0f;
         bool ok = true;
 
-        auto merge_pv = [&](int t) -> bool {          // O (this group's columns) = a_prev O + PV_t
+        // O (this group's columns) = a_prev O + PV_t.  A warp vote keeps the TMEM loads
+        // warp-uniform; a failed wait is carried into the next block-wide vote, so every
+        // softmax thread takes the same number of barrier-1 steps and leaves the loop together.
+        auto merge_pv = [&](int t) -> bool {
             const int s = t & 1;
-            const bool got = w.wait(pvfull(s), (t >> 1) & 1u, kDevErrEpilogueFull);
-            if (!named_bar_and(1, Cfg::SM_THREADS, got)) return false;
+            const bool got = __all_sync(0xffffffffu, w.wait(pvfull(s), (t >> 1) & 1u, kDevErrEpilogueFull));
+            if (!got) return false;
             tcgen05_fence_after();
 #pragma unroll
             for (int c = 0; c < DG / 32; ++c) {
@@ -257,53 +295,88 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 tmem_ld_32x32b_x32(lane_base + Cfg::T_PV + s * D + g * DG + c * 32, rr);
                 tmem_ld_wait(rr);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], a_prev, __uint_as_float(rr[i]));
+                for (int i = 0; i < 32; i += 2)
+                    fma_pair<Cfg::kPacked>(o[c * 32 + i], o[c * 32 + i + 1], o[c * 32 + i], o[c * 32 + i + 1],
+                                           a_prev, a_prev, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
             }
             tcgen05_fence_before();
             mbar_arrive(pvempty(s));
             return true;
         };
 
+        float* maxp = reinterpret_cast<float*>(smem + Cfg::OFF_MAXP);
         for (int j = 0; j < nkv; ++j) {
             const int s = j & 1;
-            const bool got = w.wait(sfull(s), (j >> 1) & 1u, kDevErrEpilogueFull);
-            if (!named_bar_and(1, Cfg::SM_THREADS, got)) {
-                ok = false;
-                break;
+            const bool got = __all_sync(0xffffffffu, w.wait(sfull(s), (j >> 1) & 1u, kDevErrEpilogueFull));
+            if constexpr (!XM) {
+                if (!named_bar_and(1, Cfg::SM_THREADS, got && ok)) {
+                    ok = false;
+                    break;
+                }
             }
             tcgen05_fence_after();
             const uint32_t s_col = lane_base + Cfg::T_S + s * 128;
             const int k0 = j * Cfg::BKV;
             const int k_lim = p.causal ? min(p.Skv, qi + p.causal_offset + 1) : p.Skv;   // keys < k_lim
             const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
-            // pass 1 (whole row): maximum of the scaled, masked scores, in log2 units.
-            // `masked` differs between rows of one warp on a diagonal tile, so the TMEM loads
-            // (.sync.aligned: the whole warp together) stay outside the branch.
-            float mt = -INFINITY, hi = -INFINITY, lo = INFINITY;
+            // pass 1: maximum of the scaled, masked scores in log2 units, over the whole row or
+            // (XM) over this group's keys.  `masked` differs between rows of one warp on a
+            // diagonal tile, so the TMEM loads (.sync.aligned) stay outside the branch.
+            float mt = -INFINITY;
+            if (got) {
+                const int first = XM ? g * KG : 0;
+                float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32(s_col + c * 32, rr);
-                tmem_ld_wait(rr);
-                if (!masked) {
+                for (int c = 0; c < P1_CHUNKS; ++c) {
+                    const int kc = first + c * 32;
+                    uint32_t rr[32];
+                    tmem_ld_32x32b_x32(s_col + kc, rr);
+                    tmem_ld_wait(rr);
+                    if (!masked) {
+                        if (scale_pos) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        hi = fmaxf(hi, __uint_as_float(rr[i]));
-                        lo = fminf(lo, __uint_as_float(rr[i]));
+                            for (int i = 0; i < 32; i += 8) {
+                                e0 = max3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
+                                e1 = max3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+                                e2 = max3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
+                                e3 = max3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 8) {
+                                e0 = min3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
+                                e1 = min3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+                                e2 = min3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
+                                e3 = min3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (k0 + kc + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * sl2);
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * p.scale_log2);
                 }
+                if (!masked)
+                    mt = (scale_pos ? max3f(fmaxf(e0, e1), e2, e3) : min3f(fminf(e0, e1), e2, e3)) * sl2;
             }
-            if (!masked) mt = (scale_pos ? hi : lo) * p.scale_log2;
+            if constexpr (XM) {
+                // partial maxima meet in shared memory (one slot per S buffer, so a slot is
+                // rewritten only after both groups have passed the next tile's barrier)
+                maxp[(s * G + g) * Cfg::BQ + r] = mt;
+                if (!named_bar_and(1, Cfg::SM_THREADS, got && ok)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg)
+                    if (gg != g) mt = fmaxf(mt, maxp[(s * G + gg) * Cfg::BQ + r]);
+            }
             const float m_new = fmaxf(m, mt);
             const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
             const float neg_m = (m_new == -INFINITY) ? 0.0f : -m_new;
             // pass 2 (this group's keys): P = 2^(x - m_new) in fp16 into shared memory
             uint8_t* prow = smem + Cfg::OFF_P + s * Cfg::P_BYTES + r * 128;
-            float lsum = 0.0f;
+            float ls0 = 0.0f, ls1 = 0.0f;
 #pragma unroll
             for (int c = 0; c < KG / 32; ++c) {
                 const int kc = g * KG + c * 32;          // first key of this 32-key slice
@@ -311,18 +384,30 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 tmem_ld_32x32b_x32(s_col + kc, rr);
                 tmem_ld_wait(rr);
                 uint32_t packed[16];
+                if (!masked) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), p.scale_log2, neg_m));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), p.scale_log2, neg_m));
-                    if (masked) {
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        fma_pair<Cfg::kPacked>(x0, x1, __uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]),
+                                               sl2, sl2, neg_m, neg_m);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        add_pair<Cfg::kPacked>(ls0, ls1, p0, p1);
+                        __half2 h = __floats2half2_rn(p0, p1);
+                        packed[i] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
                         const int kk = k0 + kc + 2 * i;
+                        float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), sl2, neg_m));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), sl2, neg_m));
                         if (kk >= k_lim || m_new == -INFINITY) p0 = 0.0f;
                         if (kk + 1 >= k_lim || m_new == -INFINITY) p1 = 0.0f;
+                        ls0 += p0;
+                        ls1 += p1;
+                        __half2 h = __floats2half2_rn(p0, p1);
+                        packed[i] = *reinterpret_cast<uint32_t*>(&h);
                     }
-                    lsum += p0 + p1;
-                    __half2 h = __floats2half2_rn(p0, p1);
-                    packed[i] = *reinterpret_cast<uint32_t*>(&h);
                 }
                 // keys kc .. kc+31: 64-key chunk kc/64, 16-byte pieces ((kc%64)/8) .. +3, swizzled by row
 #pragma unroll
@@ -340,17 +425,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             mbar_arrive(sempty(s));          // S buffer free for S_{j+2}
             fence_proxy_async_smem();
             mbar_arrive(pfull(s));           // P_j ready for the MMA
-            l = l * alpha + lsum;            // this group's part of the row sum
+            l = l * alpha + (ls0 + ls1);     // this group's part of the row sum
             m = m_new;
-            if (j >= 1 && !merge_pv(j - 1)) {
-                ok = false;
-                break;
-            }
+            if (j >= 1 && !merge_pv(j - 1)) ok = false;
             a_prev = alpha;
         }
         if (ok && nkv > 0) ok = merge_pv(nkv - 1);
-        // the row sum: group 0 adds the other groups' parts (one exchange per kernel)
-        float* lpart = reinterpret_cast<float*>(smem + Cfg::OFF_LSUM);
+        // the row sum: group 0 adds the other groups' parts (one exchange per kernel) in the
+        // S-buffer slot the last tile did not use: nobody reads it after that tile's barrier
+        float* lpart = maxp + ((((nkv - 1) & 1) ^ 1) * G) * Cfg::BQ;
         if (G > 1) {
             if (g > 0) lpart[(g - 1) * Cfg::BQ + r] = l;
             named_bar_sync(2, Cfg::SM_THREADS);

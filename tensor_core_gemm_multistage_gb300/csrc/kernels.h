@@ -18,6 +18,7 @@ enum DeviceError : int {
     kDevErrMmaAccEmpty = 3,     // MMA issuer: accumulator never released by the epilogue
     kDevErrEpilogueFull = 4,    // epilogue: accumulator never committed by the MMA issuer
     kDevErrTeardown = 5,        // teardown: in-flight copies or MMAs did not drain
+    kDevErrLayout = 6,          // dynamic shared memory not 1024-byte aligned (kernel did nothing)
     kDevErrKernelTiled = 0x100,
     kDevErrKernelSkinny = 0x200,
     kDevErrKernelAttention = 0x300,

@@ -281,6 +281,37 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Three-input maximum / minimum (one instruction on sm_100 and later; a NaN operand is
+// ignored, as with fmaxf / fminf).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float y;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
+// Packed pairs of fp32 (one instruction for two lanes of arithmetic, sm_100 and later):
+// (y0, y1) = (a0 b0 + c0, a1 b1 + c1), rounded to nearest, and (y0, y1) += (a0, a1).
+__device__ __forceinline__ void ffma2(float& y0, float& y1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& y0, float& y1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, ry;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 ry, {%0, %1};\n\t"
+        "add.rn.f32x2 ry, ry, ra;\n\tmov.b64 {%0, %1}, ry;\n\t}"
+        : "+f"(y0), "+f"(y1)
+        : "f"(a0), "f"(a1));
+}
+
 // ---------------------------------------------------------------------------
 // Epilogue arithmetic: y = max(alpha * acc, 0), rounded to fp16 (nearest even)
 // ---------------------------------------------------------------------------

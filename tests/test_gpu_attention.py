@@ -79,6 +79,19 @@ def test_explicit_scale_and_identical_keys():
     assert np.allclose(o.astype(np.float64), np.broadcast_to(mean, o.shape), atol=2e-3)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_negative_scale(D, causal):
+    # a negative scale turns the row maximum of the scaled scores into the minimum of the raw ones
+    check(*inputs(1, 2, 300, 300, D, seed=11 + D), causal=causal, scale=-0.2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_peaked_rows(causal):
+    # large scores: each row's weight sits on a few keys, often in only one of a tile's key halves
+    check(*inputs(2, 1, 384, 384, 128, seed=12), causal=causal, scale=1.5)
+
+
 def test_no_keys_and_fully_masked_rows():
     q, k, v = inputs(1, 1, 200, 70, 64, seed=4)
     check(q, k, v, causal=True)                    # rows 0..129 have no key
