@@ -11,10 +11,10 @@
 //    once, then K_j and V_j into a 2-stage ring), warp 1 issues every MMA from one lane,
 //    warps 2-9 run the softmax in two groups of four warps: each query row (TMEM lane) has
 //    one thread in each group, and each thread owns half of the row's keys and half of its
-//    output columns.  Per tile the two threads of a row exchange their partial maxima through
-//    shared memory (the block-wide vote that ends a failed wait doubles as that exchange),
-//    then each exponentiates its keys and merges its columns; the halves of the row sum are
-//    added once at the end;
+//    output columns.  Per tile the threads of a row combine their partial maxima with a
+//    shared-memory atomicMax (three rotating slots; the block-wide vote that ends a failed
+//    wait doubles as the barrier), then each exponentiates its keys (packed f32x2 arithmetic,
+//    ex2.approx) and merges its columns; the partial row sums are added once at the end;
 //  * S_j = Q K_j^T (M 128 queries, N 128 keys, K = head_dim) accumulates in TMEM, two
 //    buffers, so S_{j+1} is computed while the softmax reads S_j;
 //  * the softmax reads its S row twice from TMEM (max, then exponentials), writes P_j in
@@ -32,7 +32,7 @@
 namespace gsr {
 namespace {
 
-template <int D_>
+template <int D_, int G_>
 struct AttnCfg {
     static constexpr int D = D_;                      // head dim: 64 or 128
     static constexpr int BQ = 128, BKV = 128;
@@ -41,10 +41,10 @@ struct AttnCfg {
     static constexpr int Q_BYTES = BQ * D * 2;
     static constexpr int KV_BYTES = BKV * D * 2;
     static constexpr int P_BYTES = BQ * BKV * 2;      // 32 KB: two 64-key chunks
-    static constexpr int G = 2;                       // softmax warp groups per query row
+    static constexpr int G = G_;                      // softmax warp groups per query row
     static constexpr int SM_THREADS = 128 * G;        // softmax threads
     static constexpr int NUM_THREADS = 64 + SM_THREADS;
-    static constexpr int KEYS_PER_G = BKV / G;        // keys of a row each group exponentiates
+    static constexpr int KEYS_PER_G = BKV / G;        // keys of a row each group owns
     static constexpr int DCOLS_PER_G = D / G;         // output columns each group accumulates
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
@@ -52,10 +52,10 @@ struct AttnCfg {
     static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
     static constexpr int NUM_BARS = 1 + 9 * 2 + 1;
-    // [2 S buffers][G][128] partial row maxima; after the last tile the slot of the unused
-    // buffer carries the partial row sums
+    // three rotating slots of 128 row maxima, order-encoded as int for shared atomicMax
+    static constexpr int MAX_SLOTS = 3;
     static constexpr int OFF_MAXP = OFF_BAR + NUM_BARS * 8;
-    static constexpr int OFF_MISC = OFF_MAXP + 2 * G * BQ * 4;
+    static constexpr int OFF_MISC = OFF_MAXP + MAX_SLOTS * BQ * 4;
     // no alignment slack: the window is declared 1024-byte aligned and the kernel checks it
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int TMEM_COLS = 512;             // S 2 x 128, PV 2 x D
@@ -63,34 +63,30 @@ struct AttnCfg {
     static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q, K both K-major
     static constexpr uint32_t IDESC_PV = idesc_f16_f32(BQ, D, false, true);     // P K-major, V MN-major
 
-    static constexpr bool kExchangeMax = true;        // pass 1 over own keys + exchange
-    static constexpr bool kPacked = true;             // packed f32x2 arithmetic
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
-    static_assert(G == 1 || G == 2, "one or two softmax groups");
+    static_assert(G == 2 || G == 4, "two or four softmax groups");
+    static_assert(KEYS_PER_G % 32 == 0 && DCOLS_PER_G % 16 == 0, "TMEM load widths");
+    static_assert((G - 1) * BQ * 4 <= 2 * P_BYTES, "row-sum exchange lives in the P buffers");
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
     static_assert(T_PV + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
-// (y0, y1) = (a0 b0 + c0, a1 b1 + c1), packed into one instruction when P.
-template <bool P>
-__device__ __forceinline__ void fma_pair(float& y0, float& y1, float a0, float a1, float b0, float b1, float c0,
-                                         float c1) {
-    if constexpr (P) {
-        ffma2(y0, y1, a0, a1, b0, b1, c0, c1);
-    } else {
-        y0 = fmaf(a0, b0, c0);
-        y1 = fmaf(a1, b1, c1);
-    }
+// Order-preserving map of fp32 to int (a < b as floats <=> enc(a) < enc(b) as ints, NaN
+// aside), so that shared-memory atomicMax takes the maximum of floats; it is its own inverse.
+__device__ __forceinline__ int ord_enc(float f) {
+    const int i = __float_as_int(f);
+    return i >= 0 ? i : i ^ 0x7fffffff;
 }
-// (y0, y1) += (a0, a1)
-template <bool P>
-__device__ __forceinline__ void add_pair(float& y0, float& y1, float a0, float a1) {
-    if constexpr (P) {
-        fadd2(y0, y1, a0, a1);
-    } else {
-        y0 += a0;
-        y1 += a1;
-    }
+__device__ __forceinline__ float ord_dec(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
+
+// Loads 32 consecutive TMEM columns of this warp's 32 lanes into r[at .. at+31] (or 16).
+template <int W, int N>
+__device__ __forceinline__ void tmem_ld_at(uint32_t taddr, uint32_t (&r)[N], int at) {
+    static_assert(W == 32 || W == 16, "load width");
+    if constexpr (W == 32)
+        tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(r + at));
+    else
+        tmem_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r + at));
 }
 
 template <class Cfg>
@@ -150,6 +146,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         *abort_flag = 0u;
         fence_mbarrier_init();
     }
+    for (int i = threadIdx.x; i < Cfg::MAX_SLOTS * Cfg::BQ; i += Cfg::NUM_THREADS)
+        reinterpret_cast<int*>(smem + Cfg::OFF_MAXP)[i] = ord_enc(-INFINITY);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -262,12 +260,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax + output (warps 2-9)
+        // ------------------------------------------------------------ softmax + output (warps 2..)
         constexpr int G = Cfg::G;
         constexpr int KG = Cfg::KEYS_PER_G;
         constexpr int DG = Cfg::DCOLS_PER_G;
-        constexpr bool XM = Cfg::kExchangeMax;
-        constexpr int P1_CHUNKS = XM ? KG / 32 : Cfg::BKV / 32;   // 32-key slices pass 1 reads
+        constexpr int LDW = DG % 32 == 0 ? 32 : 16;  // TMEM load width of the PV merge
         const int quad = warp & 3;
         const int g = (warp - 2) >> 2;               // softmax group
         const int r = quad * 32 + lane;              // query row in the tile == TMEM lane
@@ -289,118 +286,110 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const bool got = __all_sync(0xffffffffu, w.wait(pvfull(s), (t >> 1) & 1u, kDevErrEpilogueFull));
             if (!got) return false;
             tcgen05_fence_after();
+            uint32_t rr[DG];
 #pragma unroll
-            for (int c = 0; c < DG / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32(lane_base + Cfg::T_PV + s * D + g * DG + c * 32, rr);
-                tmem_ld_wait(rr);
+            for (int c = 0; c < DG / LDW; ++c)
+                tmem_ld_at<LDW>(lane_base + Cfg::T_PV + s * D + g * DG + c * LDW, rr, c * LDW);
+            tmem_ld_wait(rr);
 #pragma unroll
-                for (int i = 0; i < 32; i += 2)
-                    fma_pair<Cfg::kPacked>(o[c * 32 + i], o[c * 32 + i + 1], o[c * 32 + i], o[c * 32 + i + 1],
-                                           a_prev, a_prev, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
-            }
+            for (int i = 0; i < DG; i += 2)
+                ffma2(o[i], o[i + 1], o[i], o[i + 1], a_prev, a_prev, __uint_as_float(rr[i]),
+                      __uint_as_float(rr[i + 1]));
             tcgen05_fence_before();
             mbar_arrive(pvempty(s));
             return true;
         };
 
-        float* maxp = reinterpret_cast<float*>(smem + Cfg::OFF_MAXP);
+        int* maxp = reinterpret_cast<int*>(smem + Cfg::OFF_MAXP);
+        int slot = 0;                                // this tile's row-maximum slot: j % 3
         for (int j = 0; j < nkv; ++j) {
             const int s = j & 1;
+            const int next_slot = slot == Cfg::MAX_SLOTS - 1 ? 0 : slot + 1;
             const bool got = __all_sync(0xffffffffu, w.wait(sfull(s), (j >> 1) & 1u, kDevErrEpilogueFull));
-            if constexpr (!XM) {
-                if (!named_bar_and(1, Cfg::SM_THREADS, got && ok)) {
-                    ok = false;
-                    break;
-                }
-            }
             tcgen05_fence_after();
-            const uint32_t s_col = lane_base + Cfg::T_S + s * 128;
-            const int k0 = j * Cfg::BKV;
+            const uint32_t s_col = lane_base + Cfg::T_S + s * 128 + g * KG;
+            const int k0 = j * Cfg::BKV + g * KG;        // first key this thread owns
             const int k_lim = p.causal ? min(p.Skv, qi + p.causal_offset + 1) : p.Skv;   // keys < k_lim
-            const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
-            // pass 1: maximum of the scaled, masked scores in log2 units, over the whole row or
-            // (XM) over this group's keys.  `masked` differs between rows of one warp on a
-            // diagonal tile, so the TMEM loads (.sync.aligned) stay outside the branch.
+            const bool masked = k0 + KG > k_lim;         // only the diagonal / last tile of a row
+            // pass 1: maximum of this thread's KG scores (scaled, masked, log2 units); pass 2
+            // reads them again from TMEM, which is cheaper than holding them in registers over
+            // the exchange.  `masked` differs between rows of one warp on a diagonal tile, so
+            // the TMEM loads (.sync.aligned) stay outside the branch.
+            uint32_t sv[KG];
             float mt = -INFINITY;
             if (got) {
-                const int first = XM ? g * KG : 0;
-                float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
 #pragma unroll
-                for (int c = 0; c < P1_CHUNKS; ++c) {
-                    const int kc = first + c * 32;
-                    uint32_t rr[32];
-                    tmem_ld_32x32b_x32(s_col + kc, rr);
-                    tmem_ld_wait(rr);
-                    if (!masked) {
-                        if (scale_pos) {
+                for (int c = 0; c < KG / 32; ++c) tmem_ld_at<32>(s_col + c * 32, sv, c * 32);
+                tmem_ld_wait(sv);
+                if (!masked) {
+                    float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
+                    if (scale_pos) {
 #pragma unroll
-                            for (int i = 0; i < 32; i += 8) {
-                                e0 = max3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
-                                e1 = max3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-                                e2 = max3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
-                                e3 = max3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 8) {
-                                e0 = min3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
-                                e1 = min3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-                                e2 = min3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
-                                e3 = min3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
-                            }
+                        for (int i = 0; i < KG; i += 8) {
+                            e0 = max3f(e0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+                            e1 = max3f(e1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+                            e2 = max3f(e2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
+                            e3 = max3f(e3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
                         }
+                        mt = max3f(fmaxf(e0, e1), e2, e3) * sl2;
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (k0 + kc + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * sl2);
+                        for (int i = 0; i < KG; i += 8) {
+                            e0 = min3f(e0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+                            e1 = min3f(e1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+                            e2 = min3f(e2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
+                            e3 = min3f(e3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
+                        }
+                        mt = min3f(fminf(e0, e1), e2, e3) * sl2;
                     }
-                }
-                if (!masked)
-                    mt = (scale_pos ? max3f(fmaxf(e0, e1), e2, e3) : min3f(fminf(e0, e1), e2, e3)) * sl2;
-            }
-            if constexpr (XM) {
-                // partial maxima meet in shared memory (one slot per S buffer, so a slot is
-                // rewritten only after both groups have passed the next tile's barrier)
-                maxp[(s * G + g) * Cfg::BQ + r] = mt;
-                if (!named_bar_and(1, Cfg::SM_THREADS, got && ok)) {
-                    ok = false;
-                    break;
-                }
+                } else {
 #pragma unroll
-                for (int gg = 0; gg < G; ++gg)
-                    if (gg != g) mt = fmaxf(mt, maxp[(s * G + gg) * Cfg::BQ + r]);
+                    for (int i = 0; i < KG; ++i)
+                        if (k0 + i < k_lim) mt = fmaxf(mt, __uint_as_float(sv[i]) * sl2);
+                }
             }
+            // row maximum over the groups: shared atomicMax into this tile's slot.  Slot j%3 was
+            // last read at tile j-3 (before barrier j-2) and is reset by group 0 at tile j-1,
+            // i.e. after barrier j-2 and before barrier j-1, so neither the reset nor the
+            // maxima of tile j can meet an older reader or writer.
+            if (g == 0) maxp[next_slot * Cfg::BQ + r] = ord_enc(-INFINITY);
+            atomicMax(&maxp[slot * Cfg::BQ + r], ord_enc(mt));
+            if (!named_bar_and(1, Cfg::SM_THREADS, got && ok)) {
+                ok = false;
+                break;
+            }
+            mt = ord_dec(maxp[slot * Cfg::BQ + r]);
+            slot = next_slot;
             const float m_new = fmaxf(m, mt);
             const float alpha = (m_new == -INFINITY) ? 1.0f : ex2_approx(m - m_new);
             const float neg_m = (m_new == -INFINITY) ? 0.0f : -m_new;
-            // pass 2 (this group's keys): P = 2^(x - m_new) in fp16 into shared memory
+            // pass 2: P = 2^(x - m_new) in fp16 into shared memory, 128-byte-swizzled K-major
             uint8_t* prow = smem + Cfg::OFF_P + s * Cfg::P_BYTES + r * 128;
             float ls0 = 0.0f, ls1 = 0.0f;
 #pragma unroll
             for (int c = 0; c < KG / 32; ++c) {
-                const int kc = g * KG + c * 32;          // first key of this 32-key slice
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32(s_col + kc, rr);
-                tmem_ld_wait(rr);
+                const int kc = g * KG + c * 32;          // first key of this 32-key slice in the tile
+                uint32_t sr[32];
+                tmem_ld_at<32>(s_col + c * 32, sr, 0);
+                tmem_ld_wait(sr);
                 uint32_t packed[16];
                 if (!masked) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         float x0, x1;
-                        fma_pair<Cfg::kPacked>(x0, x1, __uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]),
-                                               sl2, sl2, neg_m, neg_m);
+                        ffma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]),
+                              sl2, sl2, neg_m, neg_m);
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        add_pair<Cfg::kPacked>(ls0, ls1, p0, p1);
+                        fadd2(ls0, ls1, p0, p1);
                         __half2 h = __floats2half2_rn(p0, p1);
                         packed[i] = *reinterpret_cast<uint32_t*>(&h);
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int kk = k0 + kc + 2 * i;
-                        float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), sl2, neg_m));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), sl2, neg_m));
+                        const int kk = k0 + c * 32 + 2 * i;
+                        float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
                         if (kk >= k_lim || m_new == -INFINITY) p0 = 0.0f;
                         if (kk + 1 >= k_lim || m_new == -INFINITY) p1 = 0.0f;
                         ls0 += p0;
@@ -431,21 +420,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             a_prev = alpha;
         }
         if (ok && nkv > 0) ok = merge_pv(nkv - 1);
-        // the row sum: group 0 adds the other groups' parts (one exchange per kernel) in the
-        // S-buffer slot the last tile did not use: nobody reads it after that tile's barrier
-        float* lpart = maxp + ((((nkv - 1) & 1) ^ 1) * G) * Cfg::BQ;
-        if (G > 1) {
-            if (g > 0) lpart[(g - 1) * Cfg::BQ + r] = l;
-            named_bar_sync(2, Cfg::SM_THREADS);
-            if (g == 0) {
-                float total = l;
+        // the row sum: group 0 adds the other groups' parts (one exchange per kernel) in the P
+        // buffers, idle once the last PV product has completed (every thread waited for it)
+        float* lpart = reinterpret_cast<float*>(smem + Cfg::OFF_P);
+        if (g > 0) lpart[(g - 1) * Cfg::BQ + r] = l;
+        named_bar_sync(2, Cfg::SM_THREADS);
+        if (g == 0) {
+            float total = l;
 #pragma unroll
-                for (int gg = 1; gg < G; ++gg) total += lpart[(gg - 1) * Cfg::BQ + r];
-                lpart[r] = total;                // publish the full sum back
-            }
-            named_bar_sync(2, Cfg::SM_THREADS);
-            l = lpart[r];
+            for (int gg = 1; gg < G; ++gg) total += lpart[(gg - 1) * Cfg::BQ + r];
+            lpart[r] = total;                // publish the full sum back
         }
+        named_bar_sync(2, Cfg::SM_THREADS);
+        l = lpart[r];
         // epilogue: this group's output columns, O / l in fp16, and the log-sum-exp
         if (ok && qi < p.Sq) {
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
@@ -501,12 +488,18 @@ cudaError_t launch_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     return cudaGetLastError();
 }
 
+// Softmax warp groups per query tile for each head size.  Four groups measured slower than
+// two at both sizes: at 576 threads a thread gets 96 registers and the per-tile fixed costs
+// (TMEM load waits, the exchange) do not shrink with the work per thread.
+constexpr int kGroupsD64 = 2;
+constexpr int kGroupsD128 = 2;
+
 }  // namespace
 
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, int D, cudaStream_t stream) {
-    if (D == 64) return launch_cfg<AttnCfg<64>>(tmQ, tmK, tmV, p, stream);
-    if (D == 128) return launch_cfg<AttnCfg<128>>(tmQ, tmK, tmV, p, stream);
+    if (D == 64) return launch_cfg<AttnCfg<64, kGroupsD64>>(tmQ, tmK, tmV, p, stream);
+    if (D == 128) return launch_cfg<AttnCfg<128, kGroupsD128>>(tmQ, tmK, tmV, p, stream);
     return cudaErrorInvalidValue;
 }
 
