@@ -1,5 +1,6 @@
 // kernels.h - internal interface between the C-ABI layer (gsr_api.cu) and the kernel
-// translation units (gemm_tiled.cu, gemm_skinny.cu).  Not installed; not part of the ABI.
+// translation units (gemm_tiled.cu, gemm_pair.cu, gemm_skinny.cu, attention_fwd.cu).  Not
+// installed; not part of the ABI.
 #pragma once
 
 #include <cstdint>

@@ -1,8 +1,9 @@
 // ptx.cuh - thin inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
-// tcgen05 (TMEM alloc, MMA, commit, ld) and the shared-memory / instruction descriptors.
+// tcgen05 (TMEM alloc, MMA, commit, ld), the shared-memory / instruction descriptors, and a
+// few single-instruction arithmetic forms (ex2.approx, 3-input max/min, packed f32x2).
 //
-// Everything here is one instruction (or a short fixed sequence) per function; the
-// kernels in gemm_tiled.cuh and gemm_skinny.cuh compose them.
+// Everything here is one instruction (or a short fixed sequence) per function; the kernels
+// in gemm_tiled.cu, gemm_pair.cu, gemm_skinny.cu and attention_fwd.cu compose them.
 #pragma once
 
 #include <cstdint>
