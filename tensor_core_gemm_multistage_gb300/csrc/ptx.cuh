@@ -199,6 +199,19 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// Same, with A read from tensor memory: `a_tmem` addresses a 128-lane x (K/2)-column block
+// holding A row i in lane i, two fp16 values of consecutive k per 32-bit column (lower k in
+// the low half).  B stays a shared-memory descriptor.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -238,6 +251,30 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
 #pragma unroll
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
+
+// Stores to tensor memory, shape 32x32b: each thread of the warp writes N consecutive 32-bit
+// columns of its own lane (warp w reaches lanes 32*(w%4) .. +31).  tmem_st_wait() waits for
+// this thread's stores to complete.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Descriptors
@@ -295,8 +332,9 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
     return y;
 }
 
-// Packed pairs of fp32 (one instruction for two lanes of arithmetic, sm_100 and later):
-// (y0, y1) = (a0 b0 + c0, a1 b1 + c1), rounded to nearest, and (y0, y1) += (a0, a1).
+// Packed pairs of fp32 (one instruction for two lanes of arithmetic, sm_100 and later), all
+// rounded to nearest: (y0, y1) = (a0 b0 + c0, a1 b1 + c1); (y0, y1) = (a0 b0, a1 b1);
+// (y0, y1) += (a0, a1).
 __device__ __forceinline__ void ffma2(float& y0, float& y1, float a0, float a1, float b0, float b1,
                                       float c0, float c1) {
     asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
@@ -304,6 +342,13 @@ __device__ __forceinline__ void ffma2(float& y0, float& y1, float a0, float a1, 
         "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(y0), "=f"(y1)
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fmul2(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 __device__ __forceinline__ void fadd2(float& y0, float& y1, float a0, float a1) {
     asm("{\n\t.reg .b64 ra, ry;\n\t"
