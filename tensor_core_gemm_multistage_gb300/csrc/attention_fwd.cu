@@ -12,7 +12,7 @@
 //    one lane, warps 2-5 run the softmax of query tile 0 and warps 6-9 that of tile 1, one
 //    thread per query row (= TMEM lane) over all 128 keys of a key tile;
 //  * per query tile q, S_q(j) = Q_q K_j^T (M 128, N 128 keys, K = head_dim) lands in a
-//    128-column TMEM region; the softmax writes P_q(j) in fp16 over the first 64 columns of
+//    128-column TMEM region; the softmax writes P_q(j) in fp16 over the last 64 columns of
 //    that same region (tcgen05.st), and PV_q(j) = P_q(j) V_j reads P from TMEM (A operand)
 //    and V from shared memory (MN-major B operand), accumulating O_q in TMEM;
 //  * the MMA issue order PV_q(j-1), S_q(j) keeps each query tile's stream ordered: when
@@ -53,6 +53,7 @@ struct AttnCfg {
     static constexpr int TMEM_COLS = 512;
     // TMEM columns: S_q / P_q at 128 q, O_q at 256 + D q
     static constexpr uint32_t T_S = 0, T_O = 256;
+    static constexpr uint32_t P_COL = 64;             // P_q: upper 64 columns of the S_q region
     static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q, K both K-major
     static constexpr uint32_t IDESC_PV = idesc_f16_f32(BQ, D, false, true);     // P (TMEM), V MN-major
     // the exponent base moves only when a tile's maximum is more than this above it (log2 units)
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     return false;
                 tcgen05_fence_after();
                 const uint32_t v_s = sb + Cfg::OFF_V + s * Cfg::KV_BYTES;
-                const uint32_t p_t = tmem_base + Cfg::T_S + q * 128;
+                const uint32_t p_t = tmem_base + Cfg::T_S + q * 128 + Cfg::P_COL;
 #pragma unroll
                 for (int k = 0; k < Cfg::BKV / 16; ++k) {
                     // P: 16 keys = 8 TMEM columns per step; V: MN-major, 64-column chunks 16 KB
@@ -270,44 +271,54 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tcgen05_fence_after();
             const int k0 = j * Cfg::BKV;
             const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
-            // pass 1: maximum of the scaled, masked scores of the row, in log2 units.  `masked`
-            // differs between rows of one warp on a diagonal tile, so the TMEM loads stay
-            // outside the branch.
-            float mt = -INFINITY;
-            {
-                float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
+            // The row's 128 scores are four 32-column chunks c0..c3, handled through two
+            // register buffers so that each TMEM load overlaps the previous chunk's arithmetic.
+            // `masked` differs between rows of one warp on a diagonal tile, so every TMEM
+            // access stays outside the branches.
+            float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
+            float mt = -INFINITY;                        // masked tiles: running max, scaled
+            auto chunk_max = [&](const uint32_t (&rr)[32], int c) {
+                if (!masked) {
+                    if (scale_pos) {
 #pragma unroll
-                for (int c = 0; c < Cfg::BKV / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld_32x32b_x32(s_col + c * 32, rr);
-                    tmem_ld_wait(rr);
-                    if (!masked) {
-                        if (scale_pos) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 8) {
-                                e0 = max3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
-                                e1 = max3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-                                e2 = max3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
-                                e3 = max3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 8) {
-                                e0 = min3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
-                                e1 = min3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-                                e2 = min3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
-                                e3 = min3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
-                            }
+                        for (int i = 0; i < 32; i += 8) {
+                            e0 = max3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
+                            e1 = max3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+                            e2 = max3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
+                            e3 = max3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * sl2);
+                        for (int i = 0; i < 32; i += 8) {
+                            e0 = min3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
+                            e1 = min3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+                            e2 = min3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
+                            e3 = min3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
+                        }
                     }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * sl2);
                 }
-                if (!masked)
-                    mt = (scale_pos ? max3f(fmaxf(e0, e1), e2, e3) : min3f(fminf(e0, e1), e2, e3)) * sl2;
-            }
+            };
+            // pass 1: maximum of the scaled, masked scores of the row, in log2 units; it ends
+            // with c2 in ra and c3 in rb
+            uint32_t ra[32], rb[32];
+            tmem_ld_32x32b_x32(s_col + 0, ra);
+            tmem_ld_32x32b_x32(s_col + 32, rb);
+            tmem_ld_wait(ra);
+            reg_tie(rb);
+            chunk_max(ra, 0);
+            tmem_ld_32x32b_x32(s_col + 64, ra);
+            chunk_max(rb, 1);
+            tmem_ld_wait(ra);
+            tmem_ld_32x32b_x32(s_col + 96, rb);
+            chunk_max(ra, 2);
+            tmem_ld_wait(rb);
+            chunk_max(rb, 3);
+            if (!masked)
+                mt = (scale_pos ? max3f(fmaxf(e0, e1), e2, e3) : min3f(fminf(e0, e1), e2, e3)) * sl2;
             // lazy move of the exponent base: only by more than 2^RESCALE_LOG2 (always from -inf)
             float factor = 1.0f;
             const bool bump = mt > m + Cfg::RESCALE_LOG2;
@@ -334,14 +345,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
             }
             const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-            // pass 2: P = 2^(x - m) in fp16, packed two keys per column over S's first 64
-            // columns (chunk c's columns hold keys this thread has already read)
+            // pass 2: P = 2^(x - m) in fp16, two keys per column, chunk c to columns
+            // 64 + 16c .. +15 of the S region (scores c2 and c3 already sit in registers, so
+            // those columns are free; c0 and c1 are read again first)
             float ls0 = 0.0f, ls1 = 0.0f;
-#pragma unroll
-            for (int c = 0; c < Cfg::BKV / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32(s_col + c * 32, rr);
-                tmem_ld_wait(rr);
+            auto chunk_p = [&](const uint32_t (&rr)[32], int c) {
                 uint32_t packed[16];
                 if (!masked) {
 #pragma unroll
@@ -368,8 +376,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         packed[i] = *reinterpret_cast<uint32_t*>(&h);
                     }
                 }
-                tmem_st_32x32b_x16(s_col + c * 16, packed);
-            }
+                tmem_st_32x32b_x16(s_col + Cfg::P_COL + c * 16, packed);
+            };
+            chunk_p(ra, 2);                              // columns 96..111: scores of c3, in rb
+            tmem_ld_32x32b_x32(s_col + 0, ra);
+            chunk_p(rb, 3);                              // columns 112..127: c3
+            tmem_ld_wait(ra);
+            tmem_ld_32x32b_x32(s_col + 32, rb);
+            chunk_p(ra, 0);                              // columns 64..79: c2, consumed
+            tmem_ld_wait(rb);
+            chunk_p(rb, 1);                              // columns 80..95: c2, consumed
             tmem_st_wait();
             tcgen05_fence_before();
             mbar_arrive(pfull(q));           // P_q(j) (and a rescaled O_q) ready for the MMA

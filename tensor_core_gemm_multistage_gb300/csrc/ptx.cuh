@@ -245,6 +245,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 // Waits for this thread's outstanding tcgen05.ld; the registers are passed through so
 // the compiler cannot use them before the wait.
+// Marks registers as redefined here, so that no use moves above this point (a tcgen05.ld's
+// destinations are valid only after a later tcgen05.wait::ld).
+template <int N>
+__device__ __forceinline__ void reg_tie(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 template <int N>
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
