@@ -23,13 +23,20 @@
 namespace gsr {
 namespace {
 
+// 64-wide K sub-blocks per pipeline stage (1 or 2)
+constexpr int kPairKsub = 2;
+
 struct PairCfg {
-    static constexpr int BM = 256, BN = 256, BK = 64, STAGES = 6;
+    // BK = 64 is one TMA box of K (128 bytes); a stage holds KSUB such sub-blocks, so that the
+    // MMA issuer waits once per KSUB * 4 MMAs
+    static constexpr int BM = 256, BN = 256, BK = 64, KSUB = kPairKsub, STAGES = 6 / KSUB;
     static constexpr int HALF_M = 128, HALF_N = 128;          // per CTA
     static constexpr int NUM_THREADS = 192;
-    static constexpr int A_STAGE_BYTES = HALF_M * BK * 2;     // 16 KB
+    static constexpr int A_SUB_BYTES = HALF_M * BK * 2;       // 16 KB: one 64-wide K sub-block
     static constexpr int B_CHUNK_BYTES = BK * 64 * 2;         // 8 KB box (64 columns)
-    static constexpr int B_STAGE_BYTES = BK * HALF_N * 2;     // 16 KB
+    static constexpr int B_SUB_BYTES = BK * HALF_N * 2;       // 16 KB
+    static constexpr int A_STAGE_BYTES = KSUB * A_SUB_BYTES;
+    static constexpr int B_STAGE_BYTES = KSUB * B_SUB_BYTES;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;   // per CTA
     static constexpr int C_BUF_BYTES = HALF_M * 64 * 2;       // 16 KB staging chunk
     static constexpr int C_BUFS = 2;
@@ -126,7 +133,8 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
                 pair_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
                 const int m_row = mb * Cfg::BM + (int)rank * Cfg::HALF_M;
                 const int n_col = nb * Cfg::BN + (int)rank * Cfg::HALF_N;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                const int n_stages = (p.num_k_blocks + Cfg::KSUB - 1) / Cfg::KSUB;
+                for (int kb = 0; kb < n_stages; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
                         ok = false;
                         break;
@@ -140,16 +148,21 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
                             armed_mask |= 1u << stage;
                             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         }
-                        tma_load_2d_pair(sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES, &tmA,
-                                         leader_full, kb * Cfg::BK, m_row, pol);
-                        const uint32_t b_dst = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
-                        if (p.b_chunked) {
-                            tma_load_3d_pair(b_dst, &tmB, leader_full, 0, kb * Cfg::BK, n_col / 64, pol);
-                        } else {
 #pragma unroll
-                            for (int j = 0; j < Cfg::HALF_N / 64; ++j)
-                                tma_load_2d_pair(b_dst + j * Cfg::B_CHUNK_BYTES, &tmB, leader_full,
-                                                 n_col + j * 64, kb * Cfg::BK, pol);
+                        for (int h = 0; h < Cfg::KSUB; ++h) {
+                            // sub-block h: K columns [(KSUB kb + h) 64, +64); past K, TMA fills zeros
+                            const int k0 = (kb * Cfg::KSUB + h) * Cfg::BK;
+                            tma_load_2d_pair(sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES + h * Cfg::A_SUB_BYTES,
+                                             &tmA, leader_full, k0, m_row, pol);
+                            const uint32_t b_dst = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES + h * Cfg::B_SUB_BYTES;
+                            if (p.b_chunked) {
+                                tma_load_3d_pair(b_dst, &tmB, leader_full, 0, k0, n_col / 64, pol);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < Cfg::HALF_N / 64; ++j)
+                                    tma_load_2d_pair(b_dst + j * Cfg::B_CHUNK_BYTES, &tmB, leader_full,
+                                                     n_col + j * 64, k0, pol);
+                            }
                         }
                     }
                     if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -180,15 +193,19 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
                 if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
                 tcgen05_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::BN;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                const int n_stages = (p.num_k_blocks + Cfg::KSUB - 1) / Cfg::KSUB;
+                for (int kb = 0; kb < n_stages; ++kb) {
                     if (!w.wait(full_bar(stage), phase, kDevErrMmaFull)) { ok = false; break; }
                     tcgen05_fence_after();
                     const uint32_t a0 = sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES;
                     const uint32_t b0 = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < Cfg::BK / 16; ++k) {
-                        const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(b0 + k * 2048, Cfg::B_CHUNK_BYTES, 1024);
+                    for (int k = 0; k < Cfg::KSUB * Cfg::BK / 16; ++k) {
+                        // sub-block k / 4: A K-major (+32 bytes per 16 K), B MN-major (+2048 bytes)
+                        const uint32_t hs = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+                        const uint64_t ad = smem_desc_sw128(a0 + hs * Cfg::A_SUB_BYTES + kk * 32, 16, 1024);
+                        const uint64_t bd =
+                            smem_desc_sw128(b0 + hs * Cfg::B_SUB_BYTES + kk * 2048, Cfg::B_CHUNK_BYTES, 1024);
                         mma_f16_ss_pair(d_tmem, ad, bd, Cfg::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(stage), 0x3);
