@@ -8,7 +8,8 @@
 // role computes QK^T, another the softmax and the output), rebuilt on tcgen05:
 //
 //  * one CTA per (two 128-query tiles, batch x head); 320 threads: warp 0 issues TMA copies
-//    (both Q tiles once, then K_j and V_j into 2-stage rings), warp 1 issues every MMA from
+//    (both Q tiles once, then K_j with V_{j-1} into a 2-entry ring, one barrier per entry, so
+//    the MMA issuer waits once per key tile for both), warp 1 issues every MMA from
 //    one lane, warps 2-5 run the softmax of query tile 0 and warps 6-9 that of tile 1, one
 //    thread per query row (= TMEM lane) over all 128 keys of a key tile;
 //  * per query tile q, S_q(j) = Q_q K_j^T (M 128, N 128 keys, K = head_dim) lands in a
@@ -42,11 +43,12 @@ struct AttnCfg {
     static constexpr int KV_BYTES = BKV * D * 2;
     static constexpr int SM_THREADS = 128 * NQ;       // softmax threads
     static constexpr int NUM_THREADS = 64 + SM_THREADS;
+    // ring of 2 entries; entry e holds K_e and V_{e-1}, the two tiles step e consumes
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
-    static constexpr int NUM_BARS = 16;
+    static constexpr int NUM_BARS = 12;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     // no alignment slack: the window is declared 1024-byte aligned and the kernel checks it
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -78,17 +80,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint8_t* smem = smem_raw;
     const uint32_t sb = smem_u32(smem);
 
-    // barriers: 0 qfull | 1+s kfull | 3+s kempty | 5+s vfull | 7+s vempty | 9+q sfull |
-    //           11+q pfull | 13+q odone | 15 drain
+    // barriers: 0 qfull | 1+s full | 3+s empty | 5+q sfull | 7+q pfull | 9+q odone | 11 drain
     auto bar = [&](int i) { return sb + Cfg::OFF_BAR + 8u * i; };
-    const uint32_t qfull = bar(0), drain = bar(15);
-    auto kfull = [&](int s) { return bar(1 + s); };
-    auto kempty = [&](int s) { return bar(3 + s); };
-    auto vfull = [&](int s) { return bar(5 + s); };
-    auto vempty = [&](int s) { return bar(7 + s); };
-    auto sfull = [&](int q) { return bar(9 + q); };
-    auto pfull = [&](int q) { return bar(11 + q); };
-    auto odone = [&](int q) { return bar(13 + q); };
+    const uint32_t qfull = bar(0), drain = bar(11);
+    auto full = [&](int s) { return bar(1 + s); };
+    auto empty = [&](int s) { return bar(3 + s); };
+    auto sfull = [&](int q) { return bar(5 + q); };
+    auto pfull = [&](int q) { return bar(7 + q); };
+    auto odone = [&](int q) { return bar(9 + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 4);
 
@@ -113,10 +112,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(qfull, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(kfull(s), 1);
-            mbar_init(kempty(s), 1);
-            mbar_init(vfull(s), 1);
-            mbar_init(vempty(s), 1);
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
         }
         for (int q = 0; q < NQ; ++q) {
             mbar_init(sfull(q), 1);
@@ -146,7 +143,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && nkv_max > 0) {
             const uint64_t pol = l2_policy_evict_last();   // K and V are read by every query block
-            uint32_t armed = 0, armed_parity = 0;          // bit 0 Q, bits 1-2 K, bits 3-4 V
+            uint32_t armed = 0, armed_parity = 0;          // bit 0 Q, bits 1-2 ring entries
             const bool drop_q = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
             if (!drop_q) {
                 mbar_arrive_expect_tx(qfull, NQ * Cfg::Q_BYTES);
@@ -158,45 +155,43 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                     c * 64, q_base + q * Cfg::BQ, bh, pol);
                 armed |= 1u;
             }
-            for (int j = 0; j < nkv_max; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1u;
-                if (!w.wait(kempty(s), ph ^ 1u, kDevErrProducerEmpty)) break;
-                mbar_arrive_expect_tx(kfull(s), Cfg::KV_BYTES);
+            // entry e: K_e (e < nkv_max) and V_{e-1} (e >= 1); the last entry holds only V
+            for (int e = 0; e <= nkv_max; ++e) {
+                const int s = e & 1;
+                const uint32_t ph = (e >> 1) & 1u;
+                if (!w.wait(empty(s), ph ^ 1u, kDevErrProducerEmpty)) break;
+                const bool has_k = e < nkv_max, has_v = e >= 1;
+                mbar_arrive_expect_tx(full(s), (has_k ? Cfg::KV_BYTES : 0) + (has_v ? Cfg::KV_BYTES : 0));
+                if (has_k) {
 #pragma unroll
-                for (int c = 0; c < Cfg::DCH; ++c)
-                    tma_load_3d(sb + Cfg::OFF_K + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmK, kfull(s),
-                                c * 64, j * Cfg::BKV, bh, pol);
+                    for (int c = 0; c < Cfg::DCH; ++c)
+                        tma_load_3d(sb + Cfg::OFF_K + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmK, full(s),
+                                    c * 64, e * Cfg::BKV, bh, pol);
+                }
+                if (has_v) {
+#pragma unroll
+                    for (int c = 0; c < Cfg::DCH; ++c)
+                        tma_load_3d(sb + Cfg::OFF_V + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmV, full(s),
+                                    c * 64, (e - 1) * Cfg::BKV, bh, pol);
+                }
                 armed |= 2u << s;
                 armed_parity = (armed_parity & ~(2u << s)) | (ph << (1 + s));
-                if (!w.wait(vempty(s), ph ^ 1u, kDevErrProducerEmpty)) break;
-                mbar_arrive_expect_tx(vfull(s), Cfg::KV_BYTES);
-#pragma unroll
-                for (int c = 0; c < Cfg::DCH; ++c)
-                    tma_load_3d(sb + Cfg::OFF_V + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmV, vfull(s),
-                                c * 64, j * Cfg::BKV, bh, pol);
-                armed |= 8u << s;
-                armed_parity = (armed_parity & ~(8u << s)) | (ph << (3 + s));
             }
             // every copy started must land before the CTA may exit
             if (armed & 1u) w.drain(qfull, 0);
-            for (int s = 0; s < 2; ++s) {
-                if (armed & (2u << s)) w.drain(kfull(s), (armed_parity >> (1 + s)) & 1u);
-                if (armed & (8u << s)) w.drain(vfull(s), (armed_parity >> (3 + s)) & 1u);
-            }
+            for (int s = 0; s < 2; ++s)
+                if (armed & (2u << s)) w.drain(full(s), (armed_parity >> (1 + s)) & 1u);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && nkv_max > 0) {
-            // PV_q(t) = P_q(t) V_t accumulated into O_q.  The last user of V_t (query tile 1,
-            // which needs every key tile tile 0 needs) frees its stage; after its last key
-            // tile, O_q is published to the softmax group.
+            // PV_q(t) = P_q(t) V_t accumulated into O_q; V_t sits in ring entry t + 1, which
+            // the caller has waited for and frees after the step.  After its last key tile,
+            // O_q is published to the softmax group.
             auto issue_pv = [&](int q, int t) -> bool {
-                const int s = t & 1;
-                if (!w.wait(pfull(q), t & 1, kDevErrMmaFull) ||
-                    !w.wait(vfull(s), (t >> 1) & 1u, kDevErrMmaFull))
-                    return false;
+                const int s = (t + 1) & 1;
+                if (!w.wait(pfull(q), t & 1, kDevErrMmaFull)) return false;
                 tcgen05_fence_after();
                 const uint32_t v_s = sb + Cfg::OFF_V + s * Cfg::KV_BYTES;
                 const uint32_t p_t = tmem_base + Cfg::T_S + q * 128 + Cfg::P_COL;
@@ -208,14 +203,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     mma_f16_ts(tmem_base + Cfg::T_O + q * D, p_t + k * 8, bd, Cfg::IDESC_PV,
                                (t > 0 || k > 0) ? 1u : 0u);
                 }
-                if (q == NQ - 1 || t >= nkv[NQ - 1]) mma_commit(vempty(s));
                 if (t == (q == 0 ? nkv[0] : nkv[NQ - 1]) - 1) mma_commit(odone(q));
                 return true;
             };
             bool ok = w.wait(qfull, 0, kDevErrMmaFull);
             for (int j = 0; ok && j < nkv_max; ++j) {
                 const int s = j & 1;
-                if (!w.wait(kfull(s), (j >> 1) & 1u, kDevErrMmaFull)) {
+                if (!w.wait(full(s), (j >> 1) & 1u, kDevErrMmaFull)) {   // K_j and V_{j-1}
                     ok = false;
                     break;
                 }
@@ -237,11 +231,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit(kempty(s));
+                mma_commit(empty(s));
             }
+            // last entry: V_{nkv_max-1} for the final products of the tiles that need it
+            if (ok) ok = w.wait(full(nkv_max & 1), (nkv_max >> 1) & 1u, kDevErrMmaFull);
+            tcgen05_fence_after();
 #pragma unroll
             for (int q = 0; q < NQ; ++q)
                 if (ok && nkv[q] == nkv_max) ok = issue_pv(q, nkv_max - 1);
+            if (ok) mma_commit(empty(nkv_max & 1));
             mma_commit(drain);
             w.drain(drain, 0);
         }
