@@ -394,14 +394,26 @@ def run_gsr(args, w):
             for _ in range(args.warmup):
                 fn()
             torch.cuda.synchronize()
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            c0.record(stream)
-            for _ in range(args.steps):
-                fn()
-            c1.record(stream)
-            torch.cuda.synchronize()
-            ms = c0.elapsed_time(c1) / args.steps
+            if flush is None:
+                c0 = torch.cuda.Event(enable_timing=True)
+                c1 = torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                c1.record(stream)
+                torch.cuda.synchronize()
+                ms = c0.elapsed_time(c1) / args.steps
+            else:
+                # inputs that fit in L2: the same flush and per-call events as the library's line
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(args.steps)]
+                for i in range(args.steps):
+                    flush.zero_()
+                    evs[i][0].record(stream)
+                    fn()
+                    evs[i][1].record(stream)
+                torch.cuda.synchronize()
+                ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
             context[label] = {"ms_per_step": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12}
 
     if rank != 0:
