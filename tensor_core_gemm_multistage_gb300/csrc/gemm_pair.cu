@@ -188,6 +188,10 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
         if (rank == 0 && lane == 0) {
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true;
+            // Descriptors of stage 0, advanced by adding (byte offset >> 4) to their start-address
+            // field (bits 0-13): every operand lies below 232448 bytes, so the field cannot carry.
+            const uint64_t a_desc0 = smem_desc_sw128(sb + Cfg::OFF_A, 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(sb + Cfg::OFF_B, Cfg::B_CHUNK_BYTES, 1024);
             for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters, ++it) {
                 const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
                 if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
@@ -197,16 +201,14 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
                 for (int kb = 0; kb < n_stages; ++kb) {
                     if (!w.wait(full_bar(stage), phase, kDevErrMmaFull)) { ok = false; break; }
                     tcgen05_fence_after();
-                    const uint32_t a0 = sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES;
-                    const uint32_t b0 = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
+                    const uint64_t ad_s = a_desc0 + (uint64_t)((stage * Cfg::A_STAGE_BYTES) >> 4);
+                    const uint64_t bd_s = b_desc0 + (uint64_t)((stage * Cfg::B_STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int k = 0; k < Cfg::KSUB * Cfg::BK / 16; ++k) {
-                        // sub-block k / 4: A K-major (+32 bytes per 16 K), B MN-major (+2048 bytes)
                         const uint32_t hs = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
-                        const uint64_t ad = smem_desc_sw128(a0 + hs * Cfg::A_SUB_BYTES + kk * 32, 16, 1024);
-                        const uint64_t bd =
-                            smem_desc_sw128(b0 + hs * Cfg::B_SUB_BYTES + kk * 2048, Cfg::B_CHUNK_BYTES, 1024);
-                        mma_f16_ss_pair(d_tmem, ad, bd, Cfg::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ss_pair(d_tmem, ad_s + (uint64_t)((hs * Cfg::A_SUB_BYTES + kk * 32) >> 4),
+                                        bd_s + (uint64_t)((hs * Cfg::B_SUB_BYTES + kk * 2048) >> 4), Cfg::IDESC,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(stage), 0x3);
                     if (++stage == S) { stage = 0; phase ^= 1u; }
