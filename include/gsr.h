@@ -193,14 +193,17 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
 gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
 
 /* Kernel the library would run for these sizes on the current device: 0 = tiled
- * (one CTA per 128-row tile), 1 = small-M, 2 = tiled on CTA pairs (256 x 256
- * tiles; chosen when there is at least one full wave of such tiles). */
+ * (one CTA per 128-row tile), 1 = small-M, 2 = tiled on CTA pairs with 256 x 256
+ * tiles (chosen when there is at least one full wave of such tiles), 3 = tiled on
+ * CTA pairs with 256 x 128 tiles (instead of 2 when 256-wide tiles would leave the
+ * last wave badly filled). */
 int gsr_select_path(int64_t M, int64_t N, int64_t K);
 
 /* Forces a path for later calls (process-wide): 0 = automatic (default),
  * 1 = tiled with automatic tile width, 2 = small-M (only honoured when
  * M <= 64), 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles,
- * 5 = tiled on CTA pairs with 256 x 256 tiles.
+ * 5 = tiled on CTA pairs with 256 x 256 tiles, 6 = tiled on CTA pairs with
+ * 256 x 128 tiles.
  * For tests and measurements. */
 void gsr_set_path_override(int path);
 

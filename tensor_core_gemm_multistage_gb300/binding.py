@@ -36,8 +36,8 @@ class GsrError(RuntimeError):
         super().__init__(msg)
 
 
-PATH_AUTO, PATH_TILED, PATH_SKINNY, PATH_TILED_256, PATH_TILED_128, PATH_PAIR = 0, 1, 2, 3, 4, 5
-KERNEL_TILED, KERNEL_SKINNY, KERNEL_PAIR = 0, 1, 2
+PATH_AUTO, PATH_TILED, PATH_SKINNY, PATH_TILED_256, PATH_TILED_128, PATH_PAIR, PATH_PAIR_128 = 0, 1, 2, 3, 4, 5, 6
+KERNEL_TILED, KERNEL_SKINNY, KERNEL_PAIR, KERNEL_PAIR_128 = 0, 1, 2, 3
 
 _lock = threading.Lock()
 _lib = None

@@ -26,21 +26,25 @@ namespace {
 // 64-wide K sub-blocks per pipeline stage (1 or 2)
 constexpr int kPairKsub = 2;
 
+// BN: width of the pair's tile (256, or 128 where 256-wide tiles leave a wave badly filled)
+template <int BN_>
 struct PairCfg {
     // BK = 64 is one TMA box of K (128 bytes); a stage holds KSUB such sub-blocks, so that the
     // MMA issuer waits once per KSUB * 4 MMAs
-    static constexpr int BM = 256, BN = 256, BK = 64, KSUB = kPairKsub, STAGES = 6 / KSUB;
-    static constexpr int HALF_M = 128, HALF_N = 128;          // per CTA
+    static constexpr int BM = 256, BN = BN_, BK = 64, KSUB = kPairKsub;
+    static constexpr int HALF_M = 128, HALF_N = BN / 2;       // per CTA
     static constexpr int NUM_THREADS = 192;
     static constexpr int A_SUB_BYTES = HALF_M * BK * 2;       // 16 KB: one 64-wide K sub-block
     static constexpr int B_CHUNK_BYTES = BK * 64 * 2;         // 8 KB box (64 columns)
-    static constexpr int B_SUB_BYTES = BK * HALF_N * 2;       // 16 KB
+    static constexpr int B_SUB_BYTES = BK * HALF_N * 2;       // 16 KB (BN 256) or 8 KB
     static constexpr int A_STAGE_BYTES = KSUB * A_SUB_BYTES;
     static constexpr int B_STAGE_BYTES = KSUB * B_SUB_BYTES;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;   // per CTA
     static constexpr int C_BUF_BYTES = HALF_M * 64 * 2;       // 16 KB staging chunk
     static constexpr int C_BUFS = 2;
-    static constexpr int TMEM_COLS = 2 * BN;                  // two accumulators of 256 columns
+    // as many stages as fit beside the staging buffers (3 x 64 KB at BN 256, 4 x 48 KB at 128)
+    static constexpr int STAGES = (232448 - 1024 - 256 - C_BUFS * C_BUF_BYTES) / STAGE_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;                  // two accumulators of BN columns
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
     static constexpr int OFF_C = OFF_B + STAGES * B_STAGE_BYTES;
@@ -52,6 +56,8 @@ struct PairCfg {
     static constexpr uint32_t TEMPTY_ARRIVALS = 8;            // 4 epilogue warps x 2 CTAs
     static constexpr uint64_t ABORT_GUARD_NS = 2000000;       // see the producer's exit
 
+    static_assert(BN == 256 || BN == 128, "pair tile width");
+    static_assert(STAGES >= 3, "pipeline depth");
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
 };
 
@@ -66,10 +72,10 @@ __device__ __forceinline__ void pair_tile_coords(int t, int num_m_blocks, int nu
     nb = r / gsz;
 }
 
-__global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gsr_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const TiledParams p) {
-    using Cfg = PairCfg;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -290,61 +296,73 @@ __global__ void __launch_bounds__(PairCfg::NUM_THREADS, 1)
 
 }  // namespace
 
-int pair_smem_bytes() { return PairCfg::SMEM_BYTES; }
+namespace {
 
-// Largest number of co-resident CTA pairs, per device (0 if the query fails).
-int pair_max_active_clusters() {
-    static std::atomic<int> cache[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    int v = cache[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-    if (cudaFuncSetAttribute(gsr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairCfg::SMEM_BYTES) != cudaSuccess)
-        return 0;
+template <class Cfg>
+cudaLaunchConfig_t pair_launch_config(int clusters, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(PairCfg::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Largest number of co-resident CTA pairs, per device (0 if the query fails).
+template <class Cfg>
+int max_clusters() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaFuncSetAttribute(gsr_pair_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_launch_config<Cfg>(1, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gsr_pair_kernel, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gsr_pair_kernel<Cfg>, &cfg) != cudaSuccess) return 0;
     cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
-cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const TiledParams& p, int clusters, cudaStream_t stream) {
+template <class Cfg>
+cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                   const TiledParams& p, int clusters, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(gsr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PairCfg::SMEM_BYTES);
+        e = cudaFuncSetAttribute(gsr_pair_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(PairCfg::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gsr_pair_kernel, tmA, tmB, tmC, p);
+    cudaLaunchConfig_t cfg = pair_launch_config<Cfg>(clusters, stream, attr);
+    return cudaLaunchKernelEx(&cfg, gsr_pair_kernel<Cfg>, tmA, tmB, tmC, p);
+}
+
+}  // namespace
+
+int pair_smem_bytes(int bn) { return bn == 128 ? PairCfg<128>::SMEM_BYTES : PairCfg<256>::SMEM_BYTES; }
+
+int pair_max_active_clusters(int bn) { return bn == 128 ? max_clusters<PairCfg<128>>() : max_clusters<PairCfg<256>>(); }
+
+cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const TiledParams& p, int bn, int clusters, cudaStream_t stream) {
+    if (bn == 256) return launch<PairCfg<256>>(tmA, tmB, tmC, p, clusters, stream);
+    if (bn == 128) return launch<PairCfg<128>>(tmA, tmB, tmC, p, clusters, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gsr

@@ -231,14 +231,25 @@ gsr_status stream_state(int dev, cudaStream_t stream, size_t need_partials, size
 
 // 0: tiled, one CTA per 128 x BN tile; 1: small-M; 2: tiled on CTA pairs (256 x 256 tiles),
 // taken when there are at least as many pair tiles as half the SMs (one full wave of pairs).
+// Pair tiles 256 wide, or 128 wide when 256-wide tiles would leave the last wave badly filled:
+// estimated time ~ waves x tile cost, a 256 x 128 tile costing ~0.56 of a 256 x 256 one (half
+// the MMAs plus the fixed per-tile part), and the narrower tile must win by 5 %.
+int pair_path(int64_t M, int64_t N, int num_sms) {
+    const long long mb = (M + 255) / 256, clusters = num_sms / 2 > 0 ? num_sms / 2 : 1;
+    const long long w256 = (mb * ((N + 255) / 256) + clusters - 1) / clusters;
+    const long long w128 = (mb * ((N + 127) / 128) + clusters - 1) / clusters;
+    return 0.56 * (double)w128 < 0.95 * (double)w256 ? 3 : 2;
+}
+
 int choose_path(int64_t M, int64_t N, int num_sms) {
     const int o = g_path_override.load(std::memory_order_relaxed);
     if (o == 1 || o == 3 || o == 4) return 0;
     if (o == 5) return 2;
+    if (o == 6) return 3;
     if (o == 2 && M <= kSkinnyMaxM) return 1;
     if (M <= kSkinnyMaxM) return 1;
     const long long pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    return pair_tiles >= num_sms / 2 ? 2 : 0;
+    return pair_tiles >= num_sms / 2 ? pair_path(M, N, num_sms) : 0;
 }
 
 constexpr int kDefaultSms = 152;   // for gsr_select_path before any device is touched
@@ -290,7 +301,7 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }
 
-gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
+gsr_status run_pair(int bn, const void* A, const void* B, void* C, int M, int N, int K, float alpha,
                     const Epi& ep,
                     cudaStream_t stream, int dev, const DeviceInfo& info) {
     StreamState st;
@@ -301,7 +312,7 @@ gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, 
                          !(g_test_flags.load(std::memory_order_relaxed) & gsr::kTestNoChunkedB);
     if ((s = encode_fp16_2d(&tmA, A, M, K, 64, 128)) != GSR_OK) return s;
     if (chunked) {
-        if ((s = encode_fp16_chunked(&tmB, B, K, N, 64, 2)) != GSR_OK) return s;
+        if ((s = encode_fp16_chunked(&tmB, B, K, N, 64, bn / 128)) != GSR_OK) return s;
     } else if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) {
         return s;
     }
@@ -313,7 +324,7 @@ gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, 
     p.K = K;
     p.alpha = alpha;
     p.num_m_blocks = (M + 255) / 256;
-    p.num_n_blocks = (N + 255) / 256;
+    p.num_n_blocks = (N + bn - 1) / bn;
     p.num_k_blocks = (K + 63) / 64;
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.group_m = kGroupM / 2;
@@ -323,10 +334,10 @@ gsr_status run_pair(const void* A, const void* B, void* C, int M, int N, int K, 
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
     p.epi = ep.kind;
     p.bias = ep.bias;
-    int clusters = gsr::pair_max_active_clusters();
+    int clusters = gsr::pair_max_active_clusters(bn);
     if (clusters <= 0) clusters = info.num_sms / 2;
     if (clusters > p.num_tiles) clusters = p.num_tiles;
-    cudaError_t e = gsr::launch_pair(tmA, tmB, tmC, p, clusters, stream);
+    cudaError_t e = gsr::launch_pair(tmA, tmB, tmC, p, bn, clusters, stream);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }
 
@@ -388,7 +399,8 @@ gsr_status gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N
     if ((s = load_encoder()) != GSR_OK) return s;
     const int path = choose_path(M, N, info.num_sms);
     if (path == 1) return run_skinny(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
-    if (path == 2) return run_pair(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
+    if (path == 2 || path == 3)
+        return run_pair(path == 3 ? 128 : 256, A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
     return run_tiled(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
 }
 

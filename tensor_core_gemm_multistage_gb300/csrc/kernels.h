@@ -102,12 +102,13 @@ cudaError_t launch_attention_empty(__half* O, float* lse, long long rows, int D,
 cudaError_t launch_tiled(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                          const TiledParams& p, int bn, int grid, cudaStream_t stream);
 
-// Paired tiled path: clusters of 2 CTAs, 256 x 256 tiles, cta_group::2 MMA.
-// grid = 2 * clusters, clusters <= pair_max_active_clusters().
+// Paired tiled path: clusters of 2 CTAs, 256 x bn tiles (bn 256 or 128), cta_group::2 MMA.
+// tmB's 3-D box (when p.b_chunked) holds bn / 128 chunks of 64 columns.
+// grid = 2 * clusters, clusters <= pair_max_active_clusters(bn).
 cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const TiledParams& p, int clusters, cudaStream_t stream);
-int pair_max_active_clusters();
-int pair_smem_bytes();
+                        const TiledParams& p, int bn, int clusters, cudaStream_t stream);
+int pair_max_active_clusters(int bn);
+int pair_smem_bytes(int bn);
 
 // Skinny path (M <= 64): C^T = B^T A^T on 128-row tiles of N, K split into slabs.
 // mp is the MMA N (16, 32 or 64).

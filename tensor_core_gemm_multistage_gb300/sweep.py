@@ -8,7 +8,7 @@ static_assert), so the runtime knobs are:
 
   kernel   tiled 128x256, tiled 128x128, CTA pair 256x256, small-M (M <= 64 only)
   raster   the grouping of tile rows for L2 reuse (gsr_set_raster_group)
-  b_copy   one 3-D copy per stage for B, or two 2-D boxes (CTA-pair kernel, N % 64 == 0)
+  b_copy   3-D copies for B, or separate 64-column 2-D boxes (CTA-pair kernels, N % 64 == 0)
 
     python -m tensor_core_gemm_multistage_gb300.sweep --M 8192 --N 8192 --K 8192
 
@@ -27,7 +27,7 @@ import sys
 from . import binding as gsr
 
 KERNELS = {"tiled_128x256": gsr.PATH_TILED_256, "tiled_128x128": gsr.PATH_TILED_128,
-           "pair_256x256": gsr.PATH_PAIR, "small_m": gsr.PATH_SKINNY}
+           "pair_256x256": gsr.PATH_PAIR, "pair_256x128": gsr.PATH_PAIR_128, "small_m": gsr.PATH_SKINNY}
 RASTERS = (0, 4, 16)     # 0: the kernel's default grouping
 NO_3D_B = 2              # test flag bit 1
 
@@ -39,7 +39,7 @@ def candidates(M: int, N: int, K: int):
         if name == "small_m" and M > 64:
             continue
         rasters = (0,) if name == "small_m" else RASTERS
-        copies = ("3d", "2d") if (name == "pair_256x256" and N % 64 == 0) else ("default",)
+        copies = ("3d", "2d") if (name.startswith("pair_") and N % 64 == 0) else ("default",)
         for r in rasters:
             for c in copies:
                 out.append({"kernel": name, "path": path, "raster": r, "b_copy": c})
@@ -101,7 +101,7 @@ def sweep(M: int, N: int, K: int, alpha: float = 0.5, warmup: int = 5, iters: in
                   "TFLOP/s": 2.0 * M * N * K / (ms * 1e-3) / 1e12})
         results.append(r)
     best = min(results, key=lambda r: r["ms"])
-    auto = {0: "tiled", 1: "small_m", 2: "pair_256x256"}[gsr.select_path(M, N, K)]
+    auto = {0: "tiled", 1: "small_m", 2: "pair_256x256", 3: "pair_256x128"}[gsr.select_path(M, N, K)]
     return results, best, auto
 
 

@@ -1,5 +1,7 @@
 """The C ABI without a GPU: the library builds and loads, exports every function that
-include/gsr.h declares, and rejects bad arguments before touching CUDA."""
+include/gsr.h declares, and rejects bad arguments before touching CUDA.  The device addresses
+below are fake: every call here must be rejected before a launch (or run only where no GPU is
+present), since a launch on them would fault a real GPU."""
 import ctypes
 import os
 import re
@@ -80,8 +82,11 @@ def test_alias():
     M, N, K = 64, 64, 64
     assert gsr.gemm_scale_relu_ptr(A, B, A, M, N, K, 1.0) == gsr.Status.ERR_ALIAS
     assert gsr.gemm_scale_relu_ptr(A, B, B + 16 * 64, M, N, K, 1.0) == gsr.Status.ERR_ALIAS
-    # C ending exactly where A begins does not overlap
-    assert gsr.gemm_scale_relu_ptr(A, B, A - M * N * 2, M, N, K, 1.0) != gsr.Status.ERR_ALIAS
+    # C ending exactly where A begins does not overlap.  That call passes every check and
+    # would launch a kernel on these fake addresses, so it runs only where there is no GPU.
+    import torch
+    if not torch.cuda.is_available():
+        assert gsr.gemm_scale_relu_ptr(A, B, A - M * N * 2, M, N, K, 1.0) != gsr.Status.ERR_ALIAS
 
 
 def test_host_entry_validates_the_same_way():
@@ -96,12 +101,20 @@ def test_path_selection_and_override():
         assert gsr.select_path(64, 8, 8) == 1
         assert gsr.select_path(65, 8, 8) == gsr.KERNEL_TILED
         assert gsr.select_path(8192, 8192, 8192) == gsr.KERNEL_PAIR
+        assert gsr.select_path(16384, 14336, 4096) == gsr.KERNEL_PAIR
         assert gsr.select_path(1024, 1024, 1024) == gsr.KERNEL_TILED
+        # 96 256x256 pair tiles on 76 pairs: two waves, the second 26 % full; 192 of
+        # 256x128 fill three waves at 84 %
+        assert gsr.select_path(2000, 3000, 1000) == gsr.KERNEL_PAIR_128
+        assert gsr.select_path(4096, 4096, 4096) == gsr.KERNEL_PAIR
         gsr.set_path_override(gsr.PATH_TILED)
         assert gsr.select_path(16, 16384, 16384) == 0
         assert gsr.select_path(8192, 8192, 8192) == 0
         gsr.set_path_override(gsr.PATH_PAIR)
         assert gsr.select_path(1024, 1024, 1024) == gsr.KERNEL_PAIR
+        assert gsr.select_path(2000, 3000, 1000) == gsr.KERNEL_PAIR
+        gsr.set_path_override(gsr.PATH_PAIR_128)
+        assert gsr.select_path(8192, 8192, 8192) == gsr.KERNEL_PAIR_128
         gsr.set_path_override(gsr.PATH_SKINNY)
         assert gsr.select_path(16, 8, 8) == 1
         assert gsr.select_path(100, 8, 8) == 0      # small-M path needs M <= 64

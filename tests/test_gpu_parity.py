@@ -118,7 +118,7 @@ def test_edges_auto(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (129, 264, 72), (255, 120, 200), (257, 392, 136),
                                    (16, 16384, 1024), (640, 768, 4096)])
-@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_PAIR])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
 def test_edges_every_tiled_kernel(M, N, K, path):
     parity(M, N, K, 1.0, path=path, seed=7 * M + N + K)
 
@@ -133,14 +133,15 @@ def test_small_m_path(M, N, K):
 
 
 @pytest.mark.parametrize("name", ["square1024", "ragged2000x3000x1000"])
-@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_PAIR])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
 def test_small_workloads_on_each_tiled_kernel(name, path):
     w = WORKLOADS[name]
     parity(w.M, w.N, w.K, w.alpha, path=path)
 
 
-@pytest.mark.parametrize("M,N,K", [(512, 1024, 1024), (300, 768, 200)])
-def test_pair_kernel_with_and_without_3d_b_copies(M, N, K):
+@pytest.mark.parametrize("path", [gsr.PATH_PAIR, gsr.PATH_PAIR_128])
+@pytest.mark.parametrize("M,N,K", [(512, 1024, 1024), (300, 768, 200), (520, 192, 136)])
+def test_pair_kernel_with_and_without_3d_b_copies(M, N, K, path):
     # N % 64 == 0: B normally arrives as one 3-D copy per stage; test flag bit 1 forces the
     # two-box 2-D copies.  Both must match the oracle.
     A, B = make_inputs(M, N, K, seed=M + N + K)
@@ -148,16 +149,18 @@ def test_pair_kernel_with_and_without_3d_b_copies(M, N, K):
     for flags in (0, 2):
         gsr.set_test_flags(flags)
         try:
-            C = run_gpu(A, B, 0.5, gsr.PATH_PAIR)
+            C = run_gpu(A, B, 0.5, path)
         finally:
             gsr.set_test_flags(0)
-        check(C, ref, z, "pair flags=%d" % flags)
+        check(C, ref, z, "pair path=%d flags=%d" % (path, flags))
 
 
 def test_big_workloads_use_the_pair_kernel():
     for name in ("square8192", "llm_mlp_up"):
         w = WORKLOADS[name]
         assert gsr.select_path(w.M, w.N, w.K) == gsr.KERNEL_PAIR
+    w = WORKLOADS["ragged2000x3000x1000"]
+    assert gsr.select_path(w.M, w.N, w.K) == gsr.KERNEL_PAIR_128
 
 
 def test_skinny_workload_through_tiled_path():
@@ -191,7 +194,7 @@ def test_all_ones_is_exact(M, N, K, alpha, path):
     assert torch.all(C == float(np.float16(alpha * K)))
 
 
-@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_SKINNY, gsr.PATH_PAIR])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_SKINNY, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
 def test_one_hot_rows(path):
     M, N, K = 48, 392, 320
     rng = np.random.default_rng(4)

@@ -8,8 +8,9 @@ from tensor_core_gemm_multistage_gb300 import sweep
 def test_candidates_respect_each_kernels_limits():
     big = sweep.candidates(8192, 8192, 8192)
     kernels = {c["kernel"] for c in big}
-    assert kernels == {"tiled_128x256", "tiled_128x128", "pair_256x256"}     # no small-M at M > 64
+    assert kernels == {"tiled_128x256", "tiled_128x128", "pair_256x256", "pair_256x128"}   # no small-M at M > 64
     assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x256"} == {"3d", "2d"}
+    assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x128"} == {"3d", "2d"}
     small = sweep.candidates(16, 1000, 4096)                                    # N % 64 != 0
     assert "small_m" in {c["kernel"] for c in small}
     assert {c["b_copy"] for c in small} == {"default"}
@@ -22,4 +23,4 @@ def test_sweep_runs_every_candidate():
     results, best, auto = sweep.sweep(48, 1024, 512, iters=3, rounds=2)
     assert len(results) == len(sweep.candidates(48, 1024, 512))
     assert all(r["ms"] > 0 and len(r["ms_all"]) == 2 for r in results)
-    assert best in results and auto in ("tiled", "small_m", "pair_256x256")
+    assert best in results and auto in ("tiled", "small_m", "pair_256x256", "pair_256x128")
