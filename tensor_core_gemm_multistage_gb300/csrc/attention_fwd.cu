@@ -269,9 +269,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tcgen05_fence_after();
             const int k0 = j * Cfg::BKV;
             const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
-            // The row's 128 scores are four 32-column chunks c0..c3, handled through two
-            // register buffers so that each TMEM load overlaps the previous chunk's arithmetic.
-            // `masked` differs between rows of one warp on a diagonal tile, so every TMEM
+            // The row's 128 scores are four 32-column chunks c0..c3, all four loaded before
+            // one wait.  `masked` differs between rows of one warp on a diagonal tile, so every TMEM
             // access stays outside the branches.
             float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
             float mt = -INFINITY;                        // masked tiles: running max, scaled
@@ -300,21 +299,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * sl2);
                 }
             };
-            // pass 1: maximum of the scaled, masked scores of the row, in log2 units; it ends
-            // with c2 in ra and c3 in rb
-            uint32_t ra[32], rb[32];
-            tmem_ld_32x32b_x32(s_col + 0, ra);
-            tmem_ld_32x32b_x32(s_col + 32, rb);
-            tmem_ld_wait(ra);
-            reg_tie(rb);
-            chunk_max(ra, 0);
-            tmem_ld_32x32b_x32(s_col + 64, ra);
-            chunk_max(rb, 1);
-            tmem_ld_wait(ra);
-            tmem_ld_32x32b_x32(s_col + 96, rb);
-            chunk_max(ra, 2);
-            tmem_ld_wait(rb);
-            chunk_max(rb, 3);
+            // pass 1: maximum of the scaled, masked scores of the row, in log2 units.  The whole
+            // row (128 scores) comes into registers with one wait and stays there for pass 2.
+            uint32_t sc0[32], sc1[32], sc2[32], sc3[32];
+            tmem_ld_32x32b_x32(s_col + 0, sc0);
+            tmem_ld_32x32b_x32(s_col + 32, sc1);
+            tmem_ld_32x32b_x32(s_col + 64, sc2);
+            tmem_ld_32x32b_x32(s_col + 96, sc3);
+            tmem_ld_wait(sc0);
+            reg_tie(sc1);
+            reg_tie(sc2);
+            reg_tie(sc3);
+            chunk_max(sc0, 0);
+            chunk_max(sc1, 1);
+            chunk_max(sc2, 2);
+            chunk_max(sc3, 3);
             if (!masked)
                 mt = (scale_pos ? max3f(fmaxf(e0, e1), e2, e3) : min3f(fminf(e0, e1), e2, e3)) * sl2;
             // lazy move of the exponent base: only by more than 2^RESCALE_LOG2 (always from -inf)
@@ -325,27 +324,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 m = mt;
             }
             l *= factor;
-            if (j > 0 && __any_sync(0xffffffffu, bump)) {
-                // O_q (this warp's rows) *= factor: PV_q(j-1) completed before S_q(j) did
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld_32x32b_x32(o_col + c * 32, rr);
-                    tmem_ld_wait(rr);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float y0, y1;
-                        fmul2(y0, y1, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]), factor, factor);
-                        rr[i] = __float_as_uint(y0);
-                        rr[i + 1] = __float_as_uint(y1);
-                    }
-                    tmem_st_32x32b_x32(o_col + c * 32, rr);
-                }
-            }
             const float neg_m = (m == -INFINITY) ? 0.0f : -m;
             // pass 2: P = 2^(x - m) in fp16, two keys per column, chunk c to columns
-            // 64 + 16c .. +15 of the S region (scores c2 and c3 already sit in registers, so
-            // those columns are free; c0 and c1 are read again first)
+            // 64 + 16c .. +15 of the S region (free: every score is in registers)
             float ls0 = 0.0f, ls1 = 0.0f;
             auto chunk_p = [&](const uint32_t (&rr)[32], int c) {
                 uint32_t packed[16];
@@ -376,14 +357,28 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
                 tmem_st_32x32b_x16(s_col + Cfg::P_COL + c * 16, packed);
             };
-            chunk_p(ra, 2);                              // columns 96..111: scores of c3, in rb
-            tmem_ld_32x32b_x32(s_col + 0, ra);
-            chunk_p(rb, 3);                              // columns 112..127: c3
-            tmem_ld_wait(ra);
-            tmem_ld_32x32b_x32(s_col + 32, rb);
-            chunk_p(ra, 0);                              // columns 64..79: c2, consumed
-            tmem_ld_wait(rb);
-            chunk_p(rb, 1);                              // columns 80..95: c2, consumed
+            chunk_p(sc0, 0);
+            chunk_p(sc1, 1);
+            chunk_p(sc2, 2);
+            chunk_p(sc3, 3);
+            if (j > 0 && __any_sync(0xffffffffu, bump)) {
+                // O_q (this warp's rows) *= factor: PV_q(j-1) completed before S_q(j) did, and
+                // PV_q(j) waits for the arrival below; done after pass 2, when the scores are dead
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld_32x32b_x32(o_col + c * 32, rr);
+                    tmem_ld_wait(rr);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float y0, y1;
+                        fmul2(y0, y1, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]), factor, factor);
+                        rr[i] = __float_as_uint(y0);
+                        rr[i + 1] = __float_as_uint(y1);
+                    }
+                    tmem_st_32x32b_x32(o_col + c * 32, rr);
+                }
+            }
             tmem_st_wait();
             tcgen05_fence_before();
             mbar_arrive(pfull(q));           // P_q(j) (and a rescaled O_q) ready for the MMA
