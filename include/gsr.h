@@ -203,7 +203,7 @@ int gsr_select_path(int64_t M, int64_t N, int64_t K);
  * 1 = tiled with automatic tile width, 2 = small-M (only honoured when
  * M <= 64), 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles,
  * 5 = tiled on CTA pairs with 256 x 256 tiles, 6 = tiled on CTA pairs with
- * 256 x 128 tiles.
+ * 256 x 128 tiles, 7 = tiled with 128 x 64 tiles.
  * For tests and measurements. */
 void gsr_set_path_override(int path);
 

@@ -6,7 +6,7 @@ input generators.  Operator: "Tutorial14: 使用TileLang语言编写attention算
 and 3.
 """
 from .binding import (KERNEL_PAIR, KERNEL_PAIR_128, KERNEL_SKINNY, KERNEL_TILED, PATH_AUTO, PATH_PAIR, PATH_PAIR_128,
-                      PATH_SKINNY, PATH_TILED, PATH_TILED_128, PATH_TILED_256,
+                      PATH_SKINNY, PATH_TILED, PATH_TILED_64, PATH_TILED_128, PATH_TILED_256,
                       GsrError, Status, device_status, flash_attention_fwd, gemm_bias_gelu,
                       gemm_bias_gelu_ptr,
                       gemm_scale, gemm_scale_relu, gemm_scale_relu_host,
@@ -16,7 +16,7 @@ from .binding import (KERNEL_PAIR, KERNEL_PAIR_128, KERNEL_SKINNY, KERNEL_TILED,
 from ._build import build
 
 __all__ = [
-    "KERNEL_PAIR", "KERNEL_PAIR_128", "KERNEL_SKINNY", "KERNEL_TILED", "PATH_AUTO", "PATH_PAIR", "PATH_PAIR_128", "PATH_SKINNY", "PATH_TILED", "PATH_TILED_128", "PATH_TILED_256", "GsrError",
+    "KERNEL_PAIR", "KERNEL_PAIR_128", "KERNEL_SKINNY", "KERNEL_TILED", "PATH_AUTO", "PATH_PAIR", "PATH_PAIR_128", "PATH_SKINNY", "PATH_TILED", "PATH_TILED_64", "PATH_TILED_128", "PATH_TILED_256", "GsrError",
     "Status", "build", "device_status", "flash_attention_fwd", "gemm_bias_gelu", "gemm_bias_gelu_ptr", "gemm_scale",
     "gemm_scale_relu", "gemm_scale_relu_host",
     "gemm_scale_relu_host_ptr", "gemm_scale_relu_ptr", "last_cuda_error", "lib", "library_path",

@@ -37,6 +37,7 @@ class GsrError(RuntimeError):
 
 
 PATH_AUTO, PATH_TILED, PATH_SKINNY, PATH_TILED_256, PATH_TILED_128, PATH_PAIR, PATH_PAIR_128 = 0, 1, 2, 3, 4, 5, 6
+PATH_TILED_64 = 7
 KERNEL_TILED, KERNEL_SKINNY, KERNEL_PAIR, KERNEL_PAIR_128 = 0, 1, 2, 3
 
 _lock = threading.Lock()

@@ -7,8 +7,8 @@
 // Epilogue: scale and ReLU applied on chip before the single write-back).
 //
 // The GB300 design keeps those steps and changes how each one is carried out:
-//  * tile 128 x BN x 64 (BN = 256 or 128) instead of 64 x 64 x 32, because one tcgen05
-//    MMA covers 128 x BN x 16;
+//  * tile 128 x BN x 64 (BN = 256, 128 or 64) instead of 64 x 64 x 32, because one tcgen05
+//    MMA covers 128 x BN x 16 (the 64-wide tile is a tuning-sweep candidate);
 //  * a persistent grid (one CTA per SM) walks the tiles in grouped-M order so
 //    neighbouring CTAs share A and B panels in L2;
 //  * warp roles: warp 0 issues TMA loads into a STAGES-deep shared-memory ring
@@ -50,7 +50,8 @@ struct TiledCfg {
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
 
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
-    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+    static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
+                  "TMEM allocation must be a power of two");
     static_assert(BN % 64 == 0 && BN <= 256, "BN must be a multiple of 64, at most 256");
 };
 
@@ -252,6 +253,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
 using Cfg256 = TiledCfg<256, 4>;
 using Cfg128 = TiledCfg<128, 6>;
+using Cfg64 = TiledCfg<64, 8>;
 
 template <class Cfg>
 cudaError_t launch_cfg(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
@@ -289,12 +291,15 @@ cudaError_t launch_fill_bias_gelu(__half* C, const __half* bias, int M, int N, c
     return cudaGetLastError();
 }
 
-int tiled_smem_bytes(int bn) { return bn == 256 ? Cfg256::SMEM_BYTES : Cfg128::SMEM_BYTES; }
+int tiled_smem_bytes(int bn) {
+    return bn == 256 ? Cfg256::SMEM_BYTES : bn == 128 ? Cfg128::SMEM_BYTES : Cfg64::SMEM_BYTES;
+}
 
 cudaError_t launch_tiled(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                          const TiledParams& p, int bn, int grid, cudaStream_t stream) {
     if (bn == 256) return launch_cfg<Cfg256>(tmA, tmB, tmC, p, grid, stream);
     if (bn == 128) return launch_cfg<Cfg128>(tmA, tmB, tmC, p, grid, stream);
+    if (bn == 64) return launch_cfg<Cfg64>(tmA, tmB, tmC, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

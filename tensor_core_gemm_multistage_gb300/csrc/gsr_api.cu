@@ -241,9 +241,17 @@ int pair_path(int64_t M, int64_t N, int num_sms) {
     return 0.56 * (double)w128 < 0.95 * (double)w256 ? 3 : 2;
 }
 
+// Tile width of the one-CTA-per-tile kernel: 256 while 128 x 256 tiles fill the SMs, else
+// 128.  64-wide tiles (path override 7) are a sweep candidate only: on 1024^3 they spread
+// the K loop over twice the SMs and still took the same time (~12.3 us, of which ~5.8 us
+// is launch, setup and teardown), and they lost on every larger shape measured.
+int tiled_width(long long mb, int64_t N, int num_sms) {
+    return mb * ((N + 255) / 256) >= num_sms ? 256 : 128;
+}
+
 int choose_path(int64_t M, int64_t N, int num_sms) {
     const int o = g_path_override.load(std::memory_order_relaxed);
-    if (o == 1 || o == 3 || o == 4) return 0;
+    if (o == 1 || o == 3 || o == 4 || o == 7) return 0;
     if (o == 5) return 2;
     if (o == 6) return 3;
     if (o == 2 && M <= kSkinnyMaxM) return 1;
@@ -268,9 +276,11 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
     if (s != GSR_OK) return s;
 
     const int mb = (M + 127) / 128;
-    int bn = 256;
     const int o = g_path_override.load(std::memory_order_relaxed);
-    if (o == 4 || (o != 3 && (long long)mb * ((N + 255) / 256) < info.num_sms)) bn = 128;
+    int bn = tiled_width(mb, N, info.num_sms);
+    if (o == 3) bn = 256;
+    if (o == 4) bn = 128;
+    if (o == 7) bn = 64;
     const int nb = (N + bn - 1) / bn;
     const int kb = (K + 63) / 64;
 

@@ -6,7 +6,7 @@ configuration that fits in shared memory.  Here tile shapes and pipeline depths 
 per kernel at compile time (each kernel's shared-memory budget is checked by a
 static_assert), so the runtime knobs are:
 
-  kernel   tiled 128x256, tiled 128x128, CTA pair 256x256, small-M (M <= 64 only)
+  kernel   tiled 128x256, 128x128 or 128x64, CTA pair 256x256 or 256x128, small-M (M <= 64)
   raster   the grouping of tile rows for L2 reuse (gsr_set_raster_group)
   b_copy   3-D copies for B, or separate 64-column 2-D boxes (CTA-pair kernels, N % 64 == 0)
 
@@ -27,6 +27,7 @@ import sys
 from . import binding as gsr
 
 KERNELS = {"tiled_128x256": gsr.PATH_TILED_256, "tiled_128x128": gsr.PATH_TILED_128,
+           "tiled_128x64": gsr.PATH_TILED_64,
            "pair_256x256": gsr.PATH_PAIR, "pair_256x128": gsr.PATH_PAIR_128, "small_m": gsr.PATH_SKINNY}
 RASTERS = (0, 4, 16)     # 0: the kernel's default grouping
 NO_3D_B = 2              # test flag bit 1

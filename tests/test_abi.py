@@ -115,6 +115,9 @@ def test_path_selection_and_override():
         assert gsr.select_path(2000, 3000, 1000) == gsr.KERNEL_PAIR
         gsr.set_path_override(gsr.PATH_PAIR_128)
         assert gsr.select_path(8192, 8192, 8192) == gsr.KERNEL_PAIR_128
+        gsr.set_path_override(gsr.PATH_TILED_64)
+        assert gsr.select_path(8192, 8192, 8192) == gsr.KERNEL_TILED
+        assert gsr.select_path(16, 8, 8) == gsr.KERNEL_TILED
         gsr.set_path_override(gsr.PATH_SKINNY)
         assert gsr.select_path(16, 8, 8) == 1
         assert gsr.select_path(100, 8, 8) == 0      # small-M path needs M <= 64

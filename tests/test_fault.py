@@ -31,6 +31,7 @@ def built():
 @pytest.mark.parametrize("M,N,K,path,kernel", [(512, 1024, 1024, gsr.PATH_TILED, 0x100),
                                                (1024, 2048, 1024, gsr.PATH_PAIR, 0x100),
                                                (1024, 2048, 1024, gsr.PATH_PAIR_128, 0x100),
+                                               (300, 512, 1024, gsr.PATH_TILED_64, 0x100),
                                                (16, 4096, 8192, gsr.PATH_SKINNY, 0x200)])
 def test_timeout_is_reported_and_the_gpu_stays_usable(M, N, K, path, kernel):
     dev = torch.device("cuda", 0)

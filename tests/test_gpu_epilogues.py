@@ -59,7 +59,8 @@ def check(C, ref, label):
         assert np.linalg.norm(x - y) / ny <= 1e-3, label
 
 
-PATHS = [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_PAIR, gsr.PATH_PAIR_128, gsr.PATH_SKINNY]
+PATHS = [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_TILED_64, gsr.PATH_PAIR, gsr.PATH_PAIR_128,
+         gsr.PATH_SKINNY]
 SHAPES = [(16, 264, 1000), (40, 128, 72), (129, 264, 72), (300, 776, 520), (1000, 1000, 8)]
 
 

@@ -118,7 +118,8 @@ def test_edges_auto(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (129, 264, 72), (255, 120, 200), (257, 392, 136),
                                    (16, 16384, 1024), (640, 768, 4096)])
-@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_TILED_64, gsr.PATH_PAIR,
+                                  gsr.PATH_PAIR_128])
 def test_edges_every_tiled_kernel(M, N, K, path):
     parity(M, N, K, 1.0, path=path, seed=7 * M + N + K)
 
@@ -133,7 +134,7 @@ def test_small_m_path(M, N, K):
 
 
 @pytest.mark.parametrize("name", ["square1024", "ragged2000x3000x1000"])
-@pytest.mark.parametrize("path", [gsr.PATH_TILED, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
+@pytest.mark.parametrize("path", [gsr.PATH_TILED_128, gsr.PATH_TILED_64, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
 def test_small_workloads_on_each_tiled_kernel(name, path):
     w = WORKLOADS[name]
     parity(w.M, w.N, w.K, w.alpha, path=path)
@@ -172,6 +173,7 @@ def test_skinny_workload_through_tiled_path():
 
 @pytest.mark.parametrize("M,K,path", [(64, 64, gsr.PATH_AUTO), (130, 72, gsr.PATH_AUTO),
                                       (300, 256, gsr.PATH_TILED_128), (40, 136, gsr.PATH_SKINNY),
+                                      (200, 200, gsr.PATH_TILED_64),
                                       (520, 264, gsr.PATH_PAIR)])
 def test_identity_b_is_exact(M, K, path):
     # the sum has one non-zero term, so fp32 accumulation is exact and C must equal the
@@ -186,6 +188,7 @@ def test_identity_b_is_exact(M, K, path):
 @pytest.mark.parametrize("M,N,K,alpha,path", [(200, 264, 1000, 0.5, gsr.PATH_AUTO),
                                               (8, 64, 3000, 1.0, gsr.PATH_SKINNY),
                                               (130, 128, 2048, 1.0, gsr.PATH_TILED_256),
+                                              (260, 200, 4096, 0.5, gsr.PATH_TILED_64),
                                               (300, 520, 1000, 0.5, gsr.PATH_PAIR)])
 def test_all_ones_is_exact(M, N, K, alpha, path):
     A = torch.ones(M, K, dtype=torch.float16)

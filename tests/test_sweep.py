@@ -8,7 +8,8 @@ from tensor_core_gemm_multistage_gb300 import sweep
 def test_candidates_respect_each_kernels_limits():
     big = sweep.candidates(8192, 8192, 8192)
     kernels = {c["kernel"] for c in big}
-    assert kernels == {"tiled_128x256", "tiled_128x128", "pair_256x256", "pair_256x128"}   # no small-M at M > 64
+    assert kernels == {"tiled_128x256", "tiled_128x128", "tiled_128x64", "pair_256x256",
+                       "pair_256x128"}   # no small-M at M > 64
     assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x256"} == {"3d", "2d"}
     assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x128"} == {"3d", "2d"}
     small = sweep.candidates(16, 1000, 4096)                                    # N % 64 != 0
