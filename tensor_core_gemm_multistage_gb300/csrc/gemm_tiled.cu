@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     tcgen05_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const Waiter w{p.err, p.timeout_ns, abort_flag, kDevErrKernelTiled};
+    bool tmem_freed = false;                      // warp 1: released before the teardown
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -191,6 +192,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             // Every MMA this thread issued must finish before tensor memory is released.
             mma_commit(drain_bar);
             w.drain(drain_bar, 0);
+            // Tensor memory goes back as soon as the epilogue has read the last accumulator
+            // (its arrival on tempty), while it still writes that tile out: the release takes
+            // about a microsecond, which at the end of the kernel would add to every launch.
+            if (ok && it > 0) {
+                const uint32_t last = it - 1;
+                tmem_freed = w.wait(tempty_bar(last & 1u), (last >> 1) & 1u, kDevErrMmaAccEmpty);
+            }
+        }
+        tmem_freed = __shfl_sync(0xffffffffu, tmem_freed, 0);
+        if (tmem_freed) {
+            tcgen05_fence_after();
+            tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
         }
         __syncwarp();
     } else {
@@ -244,7 +257,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     tcgen05_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 1 && !tmem_freed) {   // an aborted run releases it here, after every role stopped
         __syncwarp();
         tcgen05_fence_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
