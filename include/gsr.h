@@ -138,10 +138,18 @@ gsr_status flash_attention_fwd(const void* Q, const void* K, const void* V, void
 /*
  * gemm_scale_relu with the operands in host memory: copies A and B host ->
  * device into the caller's device buffers dA and dB, runs gemm_scale_relu
- * into dC and copies C back device -> host, all queued on `stream`.  The host
- * buffers should be page-locked (cudaHostAlloc / pinned) for the copies to be
- * asynchronous.  hC holds the result once the stream has finished.  Sizes,
- * alignment and errors as for gemm_scale_relu; dC must not overlap dA or dB.
+ * into dC and copies C back device -> host, all ordered on `stream`: the call
+ * starts after the work already queued there, and work queued after it sees hC
+ * complete.  The host buffers should be page-locked (cudaHostAlloc / pinned) for
+ * the copies to be asynchronous.  Sizes, alignment and errors as for
+ * gemm_scale_relu; dC must not overlap dA or dB.
+ * From 2^33 flop (~8.6 GFLOP) and 1024 rows up the three parts overlap: B is copied
+ * first, then A in 2..8 chunks of rows; each chunk's product runs on `stream` as
+ * soon as its rows have landed and its rows of C go back while later chunks are
+ * copied in.  The copies then run on two library-owned streams per device (one
+ * per direction, joined to `stream` by library-owned events; created on first
+ * use, released by gsr_shutdown), and concurrent calls on one device queue their
+ * copies one call after the other.
  */
 gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* dA, void* dB,
                                 void* dC, int64_t M, int64_t N, int64_t K, float alpha,

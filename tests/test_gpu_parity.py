@@ -277,6 +277,41 @@ def test_host_entry_point_round_trip():
     check(hC.clone(), ref, z, "host")
 
 
+@pytest.mark.parametrize("M,N,K,chunk", [(1200, 1000, 1024, 0),         # below the threshold: one piece
+                                          (2000, 3000, 1000, 1024),      # 1024 rows + 976
+                                          (2500, 4096, 4096, 512),       # 4 x 512 rows + 452
+                                          (4096, 4096, 4096, 512)])      # 8 x 512 rows
+def test_host_entry_point_in_chunks(M, N, K, chunk):
+    # Large enough for the pipelined host path: B first, A's rows in chunks, each chunk's
+    # product and copy back overlapping the next chunk's copy in.  Every row must arrive.
+    A, B = make_inputs(M, N, K, seed=M + K)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    dA = torch.empty(M, K, dtype=torch.float16, device="cuda")
+    dB = torch.empty(K, N, dtype=torch.float16, device="cuda")
+    dC = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    stream = torch.cuda.Stream()
+    gsr.gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, 0.5, stream=stream)
+    stream.synchronize()
+    assert gsr.device_status(stream)[0] == gsr.Status.OK
+    C = hC.clone()
+    assert not torch.isnan(C).any()
+    if chunk == 0:
+        ref, z = oracle.gemm_scale_relu(A, B, 0.5, return_pre=True)
+        check(C, ref, z, "host")
+    else:
+        # the seeded row sample plus the first and last row of every chunk
+        edges = [e for c0 in range(0, M, chunk) for e in (c0, min(c0 + chunk, M) - 1)]
+        r = np.unique(np.concatenate([np.asarray(sample_rows(M)), np.asarray(edges)]))
+        ref, z = oracle.gemm_scale_relu(A, B, 0.5, rows=r, return_pre=True)
+        check(C[r], ref, z, "host chunks rows")
+    # a second call on the same buffers (events and copy streams reused) gives the same bytes
+    hC2 = torch.zeros_like(hC).pin_memory()
+    gsr.gemm_scale_relu_host(hA, hB, hC2, dA, dB, dC, 0.5, stream=stream)
+    stream.synchronize()
+    assert torch.equal(hC2.view(torch.int16), C.view(torch.int16))
+
+
 def test_gpu_validation_codes():
     dA = torch.empty(64, 64, dtype=torch.float16, device="cuda")
     dB = torch.empty(64, 64, dtype=torch.float16, device="cuda")
