@@ -76,7 +76,10 @@ typedef enum gsr_status {
  * allocated (or grown) on the first small-M call on the pair.  Both stay
  * until gsr_shutdown().  Calls on different streams never share them; such a
  * first call synchronises its stream and so should not be made during stream
- * capture.
+ * capture.  Once a stream has seen a call of the same kind (and size, for the
+ * small-M workspace), further calls on it only encode tensor maps on the host
+ * and launch, so they can be captured into a CUDA graph and replayed; a
+ * replay reads whatever the captured buffers hold then.
  */
 gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int64_t N,
                            int64_t K, float alpha, struct CUstream_st* stream);

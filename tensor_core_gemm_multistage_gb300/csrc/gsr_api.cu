@@ -543,17 +543,18 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
     char* c_h = static_cast<char*>(hC);
     char* c_d = static_cast<char*>(dC);
     // host -> device: after everything already queued on the caller's stream
-    if ((e = cudaEventRecord(start, st)) != cudaSuccess || (e = cudaStreamWaitEvent(hp->h2d, start, 0)) != cudaSuccess ||
+    gsr_status result = GSR_OK;
+    if ((e = cudaEventRecord(start, st)) != cudaSuccess) return cuda_fail(e);   // nothing queued yet
+    if ((e = cudaStreamWaitEvent(hp->h2d, start, 0)) != cudaSuccess ||
         (e = cudaMemcpyAsync(dB, hB, (size_t)K * N * 2, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess)
-        return cuda_fail(e);
-    for (int r = 0; r < nch; ++r) {
+        result = cuda_fail(e);
+    for (int r = 0; r < nch && result == GSR_OK; ++r) {
         const int64_t m0 = (int64_t)r * rows, mr = (M - m0 < rows) ? M - m0 : rows;
         if ((e = cudaMemcpyAsync(a_d + m0 * K * 2, a_h + m0 * K * 2, (size_t)(mr * K * 2), cudaMemcpyHostToDevice,
                                  hp->h2d)) != cudaSuccess ||
             (e = cudaEventRecord(ev_a(r), hp->h2d)) != cudaSuccess)
-            return cuda_fail(e);
+            result = cuda_fail(e);
     }
-    gsr_status result = GSR_OK;
     for (int r = 0; r < nch && result == GSR_OK; ++r) {
         const int64_t m0 = (int64_t)r * rows, mr = (M - m0 < rows) ? M - m0 : rows;
         if ((e = cudaStreamWaitEvent(st, ev_a(r), 0)) != cudaSuccess) {
@@ -567,9 +568,10 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
                                  hp->d2h)) != cudaSuccess)
             result = cuda_fail(e);
     }
-    // the caller's stream continues only after the last copy back (also after a failure,
-    // so that nothing of this call is left running unordered)
-    if ((e = cudaEventRecord(done, hp->d2h)) != cudaSuccess || (e = cudaStreamWaitEvent(st, done, 0)) != cudaSuccess)
+    // The caller's stream continues only after both copy streams (the last copy back, and on a
+    // failure whatever copies in were queued), so nothing of this call is left running unordered.
+    if ((e = cudaEventRecord(done, hp->h2d)) != cudaSuccess || (e = cudaStreamWaitEvent(hp->d2h, done, 0)) != cudaSuccess ||
+        (e = cudaEventRecord(done, hp->d2h)) != cudaSuccess || (e = cudaStreamWaitEvent(st, done, 0)) != cudaSuccess)
         return result != GSR_OK ? result : cuda_fail(e);
     return result;
 }
