@@ -54,10 +54,18 @@ struct Waiter {
 // ---------------------------------------------------------------------------
 // Epilogue functions on the fp32 accumulator
 // ---------------------------------------------------------------------------
-// GELU, tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+// GELU, tanh approximation: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3).
+// Since 0.5 (1 + tanh(u)) = 1 / (1 + e^(-2u)), it is evaluated as x / (1 + 2^(-w)) with
+// w = 2 u log2(e): one exp2 and one reciprocal on the special-function unit (~8 instructions
+// against ~25 for tanhf, which matters because the epilogue warp of TMEM lanes 32-63 shares
+// its scheduler with the MMA issuer), and no cancellation for large negative x, where
+// 1 + tanh(u) would lose its digits.  2^(-w) is capped at 2^64, where x / (1 + 2^64) is
+// already far below the smallest fp16 subnormal for any accumulator value.
 __device__ __forceinline__ float gelu_tanh(float x) {
-    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.0f + tanhf(u));
+    constexpr float kC1 = 2.0f * 0.7978845608028654f * 1.4426950408889634f;
+    constexpr float kC3 = kC1 * 0.044715f;
+    const float w = x * fmaf(kC3, x * x, kC1);
+    return __fdividef(x, 1.0f + ex2_approx(fminf(-w, 64.0f)));
 }
 
 __device__ __forceinline__ float epilogue_value(float acc, float alpha, float bias, int epi) {
