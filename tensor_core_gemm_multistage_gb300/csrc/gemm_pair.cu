@@ -15,6 +15,9 @@
 // Each SM thus moves half of B through its shared memory instead of all of it: per k-block
 // an SM stages 32 KB (not 48 KB) and its tensor core reads 32 KB (not 48 KB) of operands
 // for the same 128 x 256 x 64 of work, which is what limited the single-CTA kernel.
+// The persistent pairs walk work units: whole tiles, then, when the last wave would keep at
+// most half of the pairs busy, that wave's tiles as two 256 x 128 halves each (an N = 128
+// MMA over one 64-column chunk of B per CTA), so that twice as many pairs finish it sooner.
 #include <atomic>
 
 #include "device_common.cuh"
@@ -53,6 +56,7 @@ struct PairCfg {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+    static constexpr uint32_t IDESC_HALF = idesc_f16_f32(BM, BN / 2, false, true);   // half-width units
     static constexpr uint32_t TEMPTY_ARRIVALS = 8;            // 4 epilogue warps x 2 CTAs
     static constexpr uint64_t ABORT_GUARD_NS = 2000000;       // see the producer's exit
 
@@ -70,6 +74,19 @@ __device__ __forceinline__ void pair_tile_coords(int t, int num_m_blocks, int nu
     const int r = t - g * per_group;
     mb = first_m + r % gsz;
     nb = r / gsz;
+}
+
+// Work unit u -> tile (mb, nb) and which half of its columns (-1: the whole tile).  Units
+// below num_full are whole tiles; each later tile is split into two half-width units.
+__device__ __forceinline__ void pair_unit(int u, const TiledParams& p, int& mb, int& nb, int& half) {
+    int t = u;
+    half = -1;
+    if (u >= p.num_full) {
+        const int v = u - p.num_full;
+        t = p.num_full + (v >> 1);
+        half = v & 1;
+    }
+    pair_tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
 }
 
 template <class Cfg>
@@ -134,11 +151,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             uint32_t armed_mask = 0, armed_parity = 0;
             bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
-                int mb, nb;
-                pair_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+            for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+                int mb, nb, half;
+                pair_unit(u, p, mb, nb, half);
+                // this CTA's B columns: half of the unit's width (128 or, for a half unit, 64)
+                const int cta_cols = half < 0 ? Cfg::HALF_N : Cfg::HALF_N / 2;
+                const int chunks = cta_cols / 64;
                 const int m_row = mb * Cfg::BM + (int)rank * Cfg::HALF_M;
-                const int n_col = nb * Cfg::BN + (int)rank * Cfg::HALF_N;
+                const int n_col = nb * Cfg::BN + (half < 0 ? 0 : half * (Cfg::BN / 2)) + (int)rank * cta_cols;
+                const uint32_t pair_bytes = 2u * Cfg::KSUB * (Cfg::A_SUB_BYTES + chunks * Cfg::B_CHUNK_BYTES);
                 const int n_stages = (p.num_k_blocks + Cfg::KSUB - 1) / Cfg::KSUB;
                 for (int kb = 0; kb < n_stages; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
@@ -150,7 +171,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     } else {
                         const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
                         if (rank == 0) {
-                            mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+                            mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
                             armed_mask |= 1u << stage;
                             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         }
@@ -162,10 +183,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                              &tmA, leader_full, k0, m_row, pol);
                             const uint32_t b_dst = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES + h * Cfg::B_SUB_BYTES;
                             if (p.b_chunked) {
-                                tma_load_3d_pair(b_dst, &tmB, leader_full, 0, k0, n_col / 64, pol);
+                                // boxes of b_box_chunks 64-column chunks (1 when half units exist)
+                                for (int j = 0; j < chunks; j += p.b_box_chunks)
+                                    tma_load_3d_pair(b_dst + j * Cfg::B_CHUNK_BYTES, &tmB, leader_full, 0, k0,
+                                                     n_col / 64 + j, pol);
                             } else {
-#pragma unroll
-                                for (int j = 0; j < Cfg::HALF_N / 64; ++j)
+                                for (int j = 0; j < chunks; ++j)
                                     tma_load_2d_pair(b_dst + j * Cfg::B_CHUNK_BYTES, &tmB, leader_full,
                                                      n_col + j * 64, k0, pol);
                             }
@@ -198,11 +221,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             // field (bits 0-13): every operand lies below 232448 bytes, so the field cannot carry.
             const uint64_t a_desc0 = smem_desc_sw128(sb + Cfg::OFF_A, 16, 1024);
             const uint64_t b_desc0 = smem_desc_sw128(sb + Cfg::OFF_B, Cfg::B_CHUNK_BYTES, 1024);
-            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters, ++it) {
+            for (int u = cluster; ok && u < p.num_units; u += nclusters, ++it) {
                 const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
                 if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
                 tcgen05_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::BN;
+                const uint32_t idesc = u < p.num_full ? Cfg::IDESC : Cfg::IDESC_HALF;
                 const int n_stages = (p.num_k_blocks + Cfg::KSUB - 1) / Cfg::KSUB;
                 for (int kb = 0; kb < n_stages; ++kb) {
                     if (!w.wait(full_bar(stage), phase, kDevErrMmaFull)) { ok = false; break; }
@@ -213,7 +237,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     for (int k = 0; k < Cfg::KSUB * Cfg::BK / 16; ++k) {
                         const uint32_t hs = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
                         mma_f16_ss_pair(d_tmem, ad_s + (uint64_t)((hs * Cfg::A_SUB_BYTES + kk * 32) >> 4),
-                                        bd_s + (uint64_t)((hs * Cfg::B_SUB_BYTES + kk * 2048) >> 4), Cfg::IDESC,
+                                        bd_s + (uint64_t)((hs * Cfg::B_SUB_BYTES + kk * 2048) >> 4), idesc,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(stage), 0x3);
@@ -232,16 +256,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;
         uint32_t it = 0, cidx = 0;
-        for (int tile = cluster; tile < p.num_tiles; tile += nclusters, ++it) {
+        for (int u = cluster; u < p.num_units; u += nclusters, ++it) {
             const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
             const bool got = w.wait(tfull_bar(acc), acc_parity, kDevErrEpilogueFull);
             if (!named_bar_and(1, 128, got)) break;
             tcgen05_fence_after();
-            int mb, nb;
-            pair_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+            int mb, nb, half;
+            pair_unit(u, p, mb, nb, half);
             const int m0 = mb * Cfg::BM + (int)rank * Cfg::HALF_M;   // this CTA's rows
-            const int n0 = nb * Cfg::BN;
-            const int nchunks = (m0 < p.M) ? (min(Cfg::BN, p.N - n0) + 63) / 64 : 0;
+            const int n0 = nb * Cfg::BN + (half < 0 ? 0 : half * (Cfg::BN / 2));
+            // columns of C in this unit (a second half unit may lie wholly past N)
+            const int ncols = min(half < 0 ? Cfg::BN : Cfg::BN / 2, p.N - n0);
+            const int nchunks = (m0 < p.M && ncols > 0) ? (ncols + 63) / 64 : 0;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * Cfg::BN;
             const uint32_t leader_tempty = map_to_cta(tempty_bar(acc), 0);
             if (nchunks == 0) {

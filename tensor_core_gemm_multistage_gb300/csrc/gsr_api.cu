@@ -239,16 +239,29 @@ gsr_status stream_state(int dev, cudaStream_t stream, size_t need_partials, size
     return GSR_OK;
 }
 
+// Whole 256 x 256 tiles of a pair launch: all of them, unless the last wave would keep at
+// most half of the pairs busy; then that wave's tiles run as two 256 x 128 halves each, on
+// twice as many pairs (a half costs ~0.56-0.66 of a tile: half the MMAs, at N = 128, and 3/4
+// of the copies).
+int pair_full_tiles(int num_tiles, int clusters, int bn) {
+    if (bn != 256 || clusters <= 0) return num_tiles;
+    const int rem = num_tiles % clusters;
+    return (rem > 0 && 2 * rem <= clusters) ? num_tiles - rem : num_tiles;
+}
+
 // 0: tiled, one CTA per 128 x BN tile; 1: small-M; 2: tiled on CTA pairs (256 x 256 tiles),
 // taken when there are at least as many pair tiles as half the SMs (one full wave of pairs).
-// Pair tiles 256 wide, or 128 wide when 256-wide tiles would leave the last wave badly filled:
-// estimated time ~ waves x tile cost, a 256 x 128 tile costing ~0.56 of a 256 x 256 one (half
-// the MMAs plus the fixed per-tile part), and the narrower tile must win by 5 %.
+// Pair tiles 256 wide (with a last wave of half tiles where that helps), or 128 wide where
+// that is estimated to be faster: time ~ waves x tile cost, a 256 x 128 tile or half unit
+// costing ~0.56 of a 256 x 256 one in a wave of its own (half the MMAs plus the fixed
+// per-tile part), and the narrower tiles must win by 5 %.
 int pair_path(int64_t M, int64_t N, int num_sms) {
     const long long mb = (M + 255) / 256, clusters = num_sms / 2 > 0 ? num_sms / 2 : 1;
-    const long long w256 = (mb * ((N + 255) / 256) + clusters - 1) / clusters;
+    const long long t256 = mb * ((N + 255) / 256);
+    const long long full = pair_full_tiles((int)t256, (int)clusters, 256);
+    const double w256 = (double)(full / clusters) + (full < t256 ? 0.56 : (t256 % clusters ? 1.0 : 0.0));
     const long long w128 = (mb * ((N + 127) / 128) + clusters - 1) / clusters;
-    return 0.56 * (double)w128 < 0.95 * (double)w256 ? 3 : 2;
+    return 0.56 * (double)w128 < 0.95 * w256 ? 3 : 2;
 }
 
 // Tile width of the one-CTA-per-tile kernel: 256 while 128 x 256 tiles fill the SMs, else
@@ -308,6 +321,8 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
     p.num_n_blocks = nb;
     p.num_k_blocks = kb;
     p.num_tiles = mb * nb;
+    p.num_full = p.num_units = p.num_tiles;
+    p.b_box_chunks = 1;
     p.group_m = kGroupM;
     if (const int g = g_raster_group.load(std::memory_order_relaxed)) p.group_m = g;
     p.b_chunked = 0;
@@ -330,9 +345,14 @@ gsr_status run_pair(int bn, const void* A, const void* B, void* C, int M, int N,
     CUtensorMap tmA, tmB, tmC;
     const bool chunked = (N % 64) == 0 &&
                          !(g_test_flags.load(std::memory_order_relaxed) & gsr::kTestNoChunkedB);
+    const int num_tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+    int clusters = gsr::pair_max_active_clusters(bn);
+    if (clusters <= 0) clusters = info.num_sms / 2;
+    const int num_full = pair_full_tiles(num_tiles, clusters, bn);   // before capping at the units
+    const int box_chunks = (bn == 256 && num_full == num_tiles) ? 2 : 1;
     if ((s = encode_fp16_2d(&tmA, A, M, K, 64, 128)) != GSR_OK) return s;
     if (chunked) {
-        if ((s = encode_fp16_chunked(&tmB, B, K, N, 64, bn / 128)) != GSR_OK) return s;
+        if ((s = encode_fp16_chunked(&tmB, B, K, N, 64, box_chunks)) != GSR_OK) return s;
     } else if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) {
         return s;
     }
@@ -346,7 +366,10 @@ gsr_status run_pair(int bn, const void* A, const void* B, void* C, int M, int N,
     p.num_m_blocks = (M + 255) / 256;
     p.num_n_blocks = (N + bn - 1) / bn;
     p.num_k_blocks = (K + 63) / 64;
-    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.num_tiles = num_tiles;
+    p.num_full = num_full;
+    p.num_units = num_full + 2 * (num_tiles - num_full);
+    p.b_box_chunks = box_chunks;
     // 16 row blocks of 256 per raster group: under the power cap of long back-to-back runs it
     // beat 8 by 0.6 % on 8192^3 and 2.8 % on 16384 x 14336 x 4096, while 4 and 32 lost ~3 %
     // (the group size moves DRAM traffic, not SM cycles, so it shows only when power binds)
@@ -357,9 +380,7 @@ gsr_status run_pair(int bn, const void* A, const void* B, void* C, int M, int N,
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
     p.epi = ep.kind;
     p.bias = ep.bias;
-    int clusters = gsr::pair_max_active_clusters(bn);
-    if (clusters <= 0) clusters = info.num_sms / 2;
-    if (clusters > p.num_tiles) clusters = p.num_tiles;
+    if (clusters > p.num_units) clusters = p.num_units;
     cudaError_t e = gsr::launch_pair(tmA, tmB, tmC, p, bn, clusters, stream);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }

@@ -42,6 +42,12 @@ struct TiledParams {
     int M, N, K;
     float alpha;
     int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
+    // CTA-pair kernel at BN 256: work units [0, num_full) are whole tiles; every tile after
+    // them is two half-width units (256 x 128), so a last wave that would leave most pairs
+    // idle is spread over twice as many.  num_units = num_full + 2 (num_tiles - num_full).
+    // Other kernels: num_full = num_units = num_tiles.
+    int num_full, num_units;
+    int b_box_chunks;       // 64-column chunks per 3-D copy of B (b_chunked only)
     int* err;               // device error word
     uint64_t timeout_ns;    // bound on every mbarrier wait
     uint32_t test_flags;

@@ -103,9 +103,13 @@ def test_path_selection_and_override():
         assert gsr.select_path(8192, 8192, 8192) == gsr.KERNEL_PAIR
         assert gsr.select_path(16384, 14336, 4096) == gsr.KERNEL_PAIR
         assert gsr.select_path(1024, 1024, 1024) == gsr.KERNEL_TILED
-        # 96 256x256 pair tiles on 76 pairs: two waves, the second 26 % full; 192 of
-        # 256x128 fill three waves at 84 %
-        assert gsr.select_path(2000, 3000, 1000) == gsr.KERNEL_PAIR_128
+        # 96 256x256 pair tiles on 76 pairs: one full wave, then the other 20 tiles as 40
+        # half-width units (~1.56 tile times); 192 tiles of 256x128 need three waves (~1.68)
+        assert gsr.select_path(2000, 3000, 1000) == gsr.KERNEL_PAIR
+        # 256 tiles of 16384 x 1024 leave 28 for a last wave of halves (~3.56 tile times)
+        assert gsr.select_path(16384, 1024, 1024) == gsr.KERNEL_PAIR
+        # N = 128: a 256 x 256 tile is half empty, 256 x 128 tiles do the same work in ~0.56
+        assert gsr.select_path(20000, 128, 512) == gsr.KERNEL_PAIR_128
         assert gsr.select_path(4096, 4096, 4096) == gsr.KERNEL_PAIR
         gsr.set_path_override(gsr.PATH_TILED)
         assert gsr.select_path(16, 16384, 16384) == 0

@@ -161,7 +161,25 @@ def test_big_workloads_use_the_pair_kernel():
         w = WORKLOADS[name]
         assert gsr.select_path(w.M, w.N, w.K) == gsr.KERNEL_PAIR
     w = WORKLOADS["ragged2000x3000x1000"]
-    assert gsr.select_path(w.M, w.N, w.K) == gsr.KERNEL_PAIR_128
+    assert gsr.select_path(w.M, w.N, w.K) == gsr.KERNEL_PAIR
+
+
+@pytest.mark.parametrize("M,N,K", [(7600, 576, 264),     # 90 tiles: 76 whole, 14 split; second halves past N
+                                   (4096, 4096, 1024),   # 256 tiles: 228 whole, 28 split
+                                   (512, 1024, 1024)])   # 8 tiles, all split into 16 halves
+@pytest.mark.parametrize("flags", [0, 2])               # 3-D boxes of one chunk / 2-D boxes for B
+def test_pair_kernel_half_width_tail(M, N, K, flags):
+    # The 256 x 256 pair kernel runs a last wave that would keep at most half the pairs busy
+    # as 256 x 128 half units; a half unit past N writes nothing.
+    A, B = make_inputs(M, N, K, seed=M + 3 * N + K)
+    rows = None if M * N * K <= 2 ** 31 else sample_rows(M)
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, rows=rows, return_pre=True)
+    gsr.set_test_flags(flags)
+    try:
+        C = run_gpu(A, B, 0.5, gsr.PATH_PAIR)
+    finally:
+        gsr.set_test_flags(0)
+    check(C if rows is None else C[rows], ref, z, "half tail %dx%dx%d flags=%d" % (M, N, K, flags))
 
 
 def test_skinny_workload_through_tiled_path():
