@@ -264,12 +264,17 @@ int pair_path(int64_t M, int64_t N, int num_sms) {
     return 0.56 * (double)w128 < 0.95 * w256 ? 3 : 2;
 }
 
-// Tile width of the one-CTA-per-tile kernel: 256 while 128 x 256 tiles fill the SMs, else
-// 128.  64-wide tiles (path override 7) are a sweep candidate only: on 1024^3 they spread
-// the K loop over twice the SMs and still took the same time (~12.3 us, of which ~5.8 us
-// is launch, setup and teardown), and they lost on every larger shape measured.
+// Tile width of the one-CTA-per-tile kernel: 256 when there are at least half as many
+// 128 x 256 tiles as SMs, else 128.  An N = 256 MMA does twice the work of an N = 128 one in
+// ~1.45x the time and its tile stages less per flop, which outweighs idle SMs down to about
+// half a wave (L2 flushed, mean of 200 calls: 2048^3 with 128 tiles of 128 x 256 19.2 us
+// against 26.9 with 256 of 128 x 128, 1536 x 2048 x 2048 with 96 tiles 19.2 against 25.7),
+// but not below it (64 tiles: 1024 x 2048 x 1024 14.0 against 12.6, 512 x 4096 x 2048 18.7
+// against 17.4; 32 tiles: 1024^3 13.9 against 12.6).  64-wide tiles (path override 7) are a
+// sweep candidate only: on 1024^3 they took the same time as 128-wide ones and lost on every
+// larger shape measured.
 int tiled_width(long long mb, int64_t N, int num_sms) {
-    return mb * ((N + 255) / 256) >= num_sms ? 256 : 128;
+    return 2 * mb * ((N + 255) / 256) >= num_sms ? 256 : 128;
 }
 
 int choose_path(int64_t M, int64_t N, int num_sms) {
