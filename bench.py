@@ -41,7 +41,7 @@ from tensor_core_gemm_multistage_gb300.workloads import (ATTN_WORKLOADS, WORKLOA
                                                           workload_inputs)
 
 METRIC = "fused GEMM+scale+ReLU TFLOP/s and % of GB300 dense FP16 peak, 1 GPU"
-DEFAULT_WORKLOAD = "square8192"
+DEFAULT_WORKLOAD = "llm_mlp_up"
 L2_BYTES = 126 * 1024 * 1024
 # The sources each kernel is built from: a DRAM-traffic figure stays valid while they do.
 _SHARED_SOURCES = ["csrc/ptx.cuh", "csrc/device_common.cuh", "csrc/kernels.h"]
@@ -290,6 +290,163 @@ def config_of(w, epilogue="scale_relu"):
             if (w.M * w.K + w.K * w.N) * 2 > L2_BYTES else "flush L2 between steps"}
 
 
+def host_cpu_model() -> str:
+    """Model name of the host CPU (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_block(step, calls: int, stream, flush) -> float:
+    """Mean time of one call over `calls` back-to-back calls, CUDA events on the launching
+    stream: around the whole run, or around each call when L2 is flushed between calls."""
+    import torch
+    if flush is None:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(calls):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / calls
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(calls)]
+    for i in range(calls):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(x.elapsed_time(y) for x, y in ev) / calls
+
+
+def gemm_roofline(w, path, kernel, kernel_ms, region_ms, peaks, peaks_src):
+    """Roofline object of one GEMM workload: HBM bytes for the small-M kernel, tensor flops
+    otherwise, against the measured peak; DRAM traffic from the committed ncu summary."""
+    if path == 1:
+        achieved = w.bytes / (kernel_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+             "frac": achieved / peak, "kernel": kernel,
+             "per_launch": "%d algorithmic bytes (A+B read once, C written once)" % w.bytes}
+        key = "hbm_gbs"
+    else:
+        achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+        key = tensor_peak_key(region_ms)
+        peak = float(peaks[key])
+        r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+             "frac": achieved / peak, "kernel": kernel,
+             "per_launch": "%d algorithmic flops (2*M*N*K)" % w.flops,
+             "frac_of_burst": achieved / float(peaks["bf16_tflops"])}
+    r["traffic"] = read_traffic(w.name, kernel)
+    r["peak_source"] = "%s: %s%s" % (peaks_src, key, "" if path == 1 else
+                                     "; fp16 dense rate taken equal to the bf16 rate (nominal ratio 1)")
+    return r
+
+
+def time_gemm(gsr, w, args, dev, stream, world, epilogue="scale_relu"):
+    """Warm-up, then exactly args.steps calls timed with CUDA events on the launching stream
+    (per call and around the whole region), between barriers and synchronisations.  Inputs
+    that fit in L2 are evicted before every call by a 256 MiB write outside the call's events.
+    Returns the timing record and the device inputs (for the e2e leg)."""
+    import torch
+
+    A, B = workload_inputs(w)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.empty(w.M, w.N, dtype=torch.float16, device=dev)
+    inputs_bytes = (w.M * w.K + w.K * w.N) * 2
+    flush = None
+    if inputs_bytes <= L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    if epilogue == "bias_gelu":
+        from tensor_core_gemm_multistage_gb300.workloads import make_bias
+        dbias = make_bias(w.N, seed=1).to(dev)
+
+        def step():
+            gsr.gemm_bias_gelu(dA, dB, dbias, dC, stream=stream)
+    elif epilogue == "scale":
+        def step():
+            gsr.gemm_scale(dA, dB, dC, w.alpha, stream=stream)
+    else:
+        def step():
+            gsr.gemm_scale_relu(dA, dB, dC, w.alpha, stream=stream)
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    torch.cuda.synchronize()
+    status, code = gsr.device_status(stream)
+    if status != gsr.Status.OK:
+        raise RuntimeError("%s: device status %s code %#x" % (w.name, status.name, code))
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    region_ms = start.elapsed_time(stop)
+    step_ms = region_ms / args.steps if flush is None else sum(kernel_ms) / args.steps
+    med = None
+    if args.repeats > 0:
+        # After the timed region: `repeats` more runs of max(100, steps) back-to-back calls
+        # each, timed the same way; the median of their mean call times.
+        reps = [run_block(step, max(100, args.steps), stream, flush) for _ in range(args.repeats)]
+        med = statistics.median(reps)
+    rec = {
+        "step_ms": max_over_ranks(step_ms, world),
+        "kernel_ms": max_over_ranks(sum(kernel_ms) / len(kernel_ms), world),
+        "median5_ms": max_over_ranks(med, world) if med is not None else None,
+        "region_ms": region_ms, "wall": (t_wall0, t_wall1),
+        "l2": ("inputs larger than L2 (A+B %d MiB > 126 MiB), no flush" % (inputs_bytes >> 20))
+        if flush is None else "flush L2 between steps (256 MiB write outside each call's events)",
+    }
+    return rec, (A, B, dA, dB, dC, flush, step)
+
+
+def per_config_entry(w, rec, path, kernel, peaks, peaks_src, world):
+    value = whole_job_tflops(world, w.flops, rec["step_ms"])
+    e = {"M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha, "kernel": kernel,
+         "ms_per_step": rec["step_ms"], "kernel_ms": rec["kernel_ms"], "TFLOP/s": value,
+         "median5_ms": rec["median5_ms"],
+         "median5_TFLOP/s": (whole_job_tflops(world, w.flops, rec["median5_ms"])
+                             if rec["median5_ms"] else None),
+         "l2": rec["l2"],
+         "roofline": gemm_roofline(w, path, kernel, rec["kernel_ms"], rec["region_ms"], peaks,
+                                   peaks_src)}
+    if path == 1:
+        e["GB/s"] = w.bytes / (rec["kernel_ms"] * 1e-3) / 1e9
+    return e
+
+
 def run_gsr(args, w):
     import torch
 
@@ -302,65 +459,15 @@ def run_gsr(args, w):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     gsr.build()
-
-    A, B = workload_inputs(w)
-    dA, dB = A.to(dev), B.to(dev)
-    dC = torch.empty(w.M, w.N, dtype=torch.float16, device=dev)
-    inputs_bytes = (w.M * w.K + w.K * w.N) * 2
-    flush = None
-    if inputs_bytes <= L2_BYTES:
-        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     path = gsr.select_path(w.M, w.N, w.K)
     kernel = KERNEL_NAMES[path]
+    peaks, peaks_src = measured_peaks()
 
-    if args.epilogue == "bias_gelu":
-        from tensor_core_gemm_multistage_gb300.workloads import make_bias
-        dbias = make_bias(w.N, seed=1).to(dev)
-
-        def step():
-            gsr.gemm_bias_gelu(dA, dB, dbias, dC, stream=stream)
-    elif args.epilogue == "scale":
-        def step():
-            gsr.gemm_scale(dA, dB, dC, w.alpha, stream=stream)
-    else:
-        def step():
-            gsr.gemm_scale_relu(dA, dB, dC, w.alpha, stream=stream)
-
-    sampler = ClockSampler(gpu_uuid()).start() if rank == 0 else None
-    for _ in range(args.warmup):
-        if flush is not None:
-            flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    t_wall0 = time.time()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    stop.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier(world)
-    status, code = gsr.device_status(stream)
-    if status != gsr.Status.OK:
-        raise RuntimeError("device status %s code %#x" % (status.name, code))
-
-    kernel_ms = [a.elapsed_time(b) for a, b in ev]
-    region_ms = start.elapsed_time(stop)
-    step_ms = region_ms / args.steps if flush is None else sum(kernel_ms) / args.steps
-    step_ms = max_over_ranks(step_ms, world)
-    kernel_avg_ms = max_over_ranks(sum(kernel_ms) / len(kernel_ms), world)
+    sampler = ClockSampler(gpu_uuid(), interval_ms=50).start() if rank == 0 else None
+    rec, (A, B, dA, dB, dC, flush, step) = time_gemm(gsr, w, args, dev, stream, world, args.epilogue)
+    t_wall0, t_wall1 = rec["wall"]
+    inputs_bytes = (w.M * w.K + w.K * w.N) * 2
 
     # end-to-end through the host entry point: pinned host in, pinned host out
     e2e = None
@@ -381,8 +488,7 @@ def run_gsr(args, w):
         e2e = {"value": whole_job_tflops(world, w.flops, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": inputs_bytes, "d2h_bytes_per_step": w.M * w.N * 2,
                "ms_per_step": e2e_ms, "steps": args.e2e_steps}
-    if sampler is not None:
-        sampler.stop()
+        del hA, hB, hC
 
     # Context only (the tutorial compares its fused kernel with unfused PyTorch): the same
     # workload as torch.relu((A @ B) * alpha) and as a plain cuBLAS fp16 matmul.
@@ -394,70 +500,78 @@ def run_gsr(args, w):
             for _ in range(args.warmup):
                 fn()
             torch.cuda.synchronize()
-            if flush is None:
-                c0 = torch.cuda.Event(enable_timing=True)
-                c1 = torch.cuda.Event(enable_timing=True)
-                c0.record(stream)
-                for _ in range(args.steps):
-                    fn()
-                c1.record(stream)
-                torch.cuda.synchronize()
-                ms = c0.elapsed_time(c1) / args.steps
-            else:
-                # inputs that fit in L2: the same flush and per-call events as the library's line
-                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                       for _ in range(args.steps)]
-                for i in range(args.steps):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for i in range(args.steps):
+                if flush is not None:
                     flush.zero_()
-                    evs[i][0].record(stream)
-                    fn()
-                    evs[i][1].record(stream)
-                torch.cuda.synchronize()
-                ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+                evs[i][0].record(stream)
+                fn()
+                evs[i][1].record(stream)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            ms = (c0.elapsed_time(c1) / args.steps if flush is None
+                  else sum(a.elapsed_time(b) for a, b in evs) / args.steps)
             context[label] = {"ms_per_step": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12}
+    del dA, dB, dC, flush, step
+
+    # The other configurations, measured the same way in the same process (same steps and
+    # warm-up): each is its own JSON object under "per_config".
+    per_config = {}
+    if args.per_config and args.epilogue == "scale_relu":
+        for name, ow in WORKLOADS.items():
+            if name == w.name:
+                continue
+            opath = gsr.select_path(ow.M, ow.N, ow.K)
+            orec, bufs = time_gemm(gsr, ow, args, dev, stream, world)
+            del bufs
+            per_config[name] = per_config_entry(ow, orec, opath, KERNEL_NAMES[opath], peaks,
+                                                peaks_src, world)
+            torch.cuda.empty_cache()
+    if sampler is not None:
+        sampler.stop()
 
     if rank != 0:
         return 0
 
-    peaks, peaks_src = measured_peaks()
-    value = whole_job_tflops(world, w.flops, step_ms)
-    if path == 1:
-        achieved = w.bytes / (kernel_avg_ms * 1e-3) / 1e9
-        peak = float(peaks["hbm_gbs"])
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "kernel": kernel,
-                    "per_launch": "%d algorithmic bytes (A+B read once, C written once)" % w.bytes}
-    else:
-        achieved = w.flops / (kernel_avg_ms * 1e-3) / 1e12
-        peak_key = tensor_peak_key(region_ms)
-        peak = float(peaks[peak_key])
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "kernel": kernel,
-                    "per_launch": "%d algorithmic flops (2*M*N*K)" % w.flops,
-                    "frac_of_burst": achieved / float(peaks["bf16_tflops"])}
-    roofline["traffic"] = read_traffic(w.name, kernel)
-    roofline["peak_source"] = ("%s: %s; fp16 dense rate taken equal to the bf16 rate "
-                               "(nominal ratio 1)" % (peaks_src, "hbm_gbs" if path == 1 else peak_key))
+    value = whole_job_tflops(world, w.flops, rec["step_ms"])
+    roofline = gemm_roofline(w, path, kernel, rec["kernel_ms"], rec["region_ms"], peaks, peaks_src)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["step_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded randn, fp16)", "config": config_of(w, args.epilogue),
         "roofline": roofline,
-        "kernel_ms": kernel_avg_ms,
+        "kernel_ms": rec["kernel_ms"],
+        "median5": {"ms_per_step": rec["median5_ms"],
+                    "TFLOP/s": (whole_job_tflops(world, w.flops, rec["median5_ms"])
+                                if rec["median5_ms"] else None),
+                    "how": "after the timed region: median over %d repeats of the mean call "
+                           "time of %d back-to-back calls" % (args.repeats, max(100, args.steps))},
         "gpu_launches": args.steps,
     }
     if e2e is not None:
         line["e2e"] = e2e
     if context is not None:
         line["context"] = context
+    if per_config:
+        line["per_config"] = per_config
     if sampler is not None:
         line["clocks"] = sampler.summary(t_wall0, t_wall1)
     if world == 1 and args.cpu_seconds > 0:
         rows, secs, cores = time_oracle(A, B, w.alpha, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": 2.0 * rows * w.N * w.K / secs / 1e12, "unit": "TFLOP/s",
-                                "cores": cores, "kind": "oracle",
-                                "sample": "%d whole rows of C (of %d), %.1f s" % (rows, w.M, secs)}
+        per_row_s = secs / rows
+        line["cpu_baseline"] = {
+            "value": 2.0 * rows * w.N * w.K / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": "%d whole rows of C (of %d), %.1f s" % (rows, w.M, secs),
+            "per_row_ms": per_row_s * 1e3,
+            "extrapolated_full_s": per_row_s * w.M,
+            "extrapolated_note": "extrapolated: measured per-row time x M rows, not a full run",
+            "cpu_model": host_cpu_model()}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -583,6 +697,10 @@ def main(argv=None):
     ap.add_argument("--epilogue", choices=["scale_relu", "scale", "bias_gelu"], default="scale_relu",
                     help="scale_relu: the fused operator (default); scale: alpha*A@B; "
                          "bias_gelu: GELU(A@B + bias)")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="repeats of max(100, steps) calls after the timed region (median reported)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="time only the selected workload, not the other four GEMM configurations")
     ap.add_argument("--torch-context", action="store_true",
                     help="also time torch.relu((A@B)*alpha) and a plain cuBLAS matmul (context)")
     args = ap.parse_args(argv)

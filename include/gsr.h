@@ -74,7 +74,7 @@ typedef enum gsr_status {
  * pair it allocates a 4-byte error word for that stream, and the small-M
  * kernel keeps fp32 partial tiles and per-tile ticket counters in a workspace
  * allocated (or grown) on the first small-M call on the pair.  Both stay
- * until gsr_shutdown().  Calls on different streams never share them; such a
+ * until gsr_release_stream() for that stream or gsr_shutdown().  Calls on different streams never share them; such a
  * first call synchronises its stream and so should not be made during stream
  * capture.  Once a stream has seen a call of the same kind (and size, for the
  * small-M workspace), further calls on it only encode tensor maps on the host
@@ -168,32 +168,46 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
  *
  * Arguments, layout, ownership and result are those of gemm_scale_relu, for
  * the small-M kernel only: 1 <= M <= 64 (M > 64 returns GSR_ERR_INVALID_ARG;
- * M == 0 or N == 0 is a no-op and K == 0 clears C, as there).  The caller
+ * M == 0 or N == 0 is a no-op and K == 0 clears C, as there).  The small-M kernel
+ * has no raster order to set: gsr_set_raster_group does not apply to it.  The caller
  * passes A, B and C; the kernel's scratch (error word, per-tile tickets and
  * split-K partial tiles) lives in one fixed 12 MiB array inside the library,
  * which every GPU that loads the library holds until the process exits.
  * Sizes whose scratch would not fit return GSR_ERR_SCRATCH_LIMIT before any
- * work is queued; on a 152-SM GB300 that happens only for N above about 4.0e8.
- * The call never runs cudaMalloc, cudaFree or any other allocating routine.
+ * work is queued; on a 152-SM GB300 that happens only for N above about 4.0e8
+ * (sizes whose per-tile tickets alone cannot fit are refused before any CUDA
+ * call).  The call never runs cudaMalloc, cudaFree or any other allocating
+ * routine.
  *
- * The first call on a device looks up the array's device address (one-time
- * set-up with that device current); make that first call before any stream
- * capture.  Every call shares the array and it keeps the last call's
- * contents; each call clears the parts that must start at zero, on `stream`,
- * before its kernel.  Calls whose work overlaps on the GPU (for example on two
- * streams with no ordering between them) race on the array and produce wrong
- * results: order them on one stream.  A bounded-wait timeout inside this
- * variant is not reported through gsr_device_status.
+ * Set-up: the first call on each device, with that device current, looks up the
+ * array's device address and makes the kernel variants resident.  Under CUDA's
+ * default lazy module loading, that is when the driver places the array and the
+ * kernels' code on the device: an allocation by the driver, which can also
+ * synchronise.  A caller with a fixed memory plan should therefore make one call
+ * on each device during start-up, and before any stream capture.  Later calls
+ * place nothing.
+ *
+ * Every call shares the array and it keeps the last call's contents; each call
+ * clears the parts that must start at zero, on `stream`, before its kernel.
+ * Calls whose work overlaps on the GPU (for example on two streams with no
+ * ordering between them) race on the array and produce wrong results: order
+ * them on one stream.  If a bounded wait inside the kernel runs out, C is left
+ * unspecified; gsr_device_status (on any stream of that device) reports
+ * GSR_ERR_DEVICE_TIMEOUT for the most recent call of this entry point there,
+ * until it has been read once or the next call starts.
  */
 gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
                                    int64_t K, float alpha, struct CUstream_st* stream);
 
 /*
  * Waits for `stream`, then reads and clears the error word of the (current
- * device, stream) pair.  Returns GSR_ERR_DEVICE_TIMEOUT if a kernel queued on
- * that stream since the last call gave up on a bounded wait (the pair's
- * small-M ticket counters are then reset too), GSR_ERR_CUDA if the stream
- * reported an error, else GSR_OK.  `code` (may be NULL) receives the raw
+ * device, stream) pair, and that of gemm_scale_relu_noalloc on the current device.
+ * Returns GSR_ERR_DEVICE_TIMEOUT if a kernel queued on that stream since the last
+ * call (or the latest gemm_scale_relu_noalloc call on the device) gave up on a
+ * bounded wait, GSR_ERR_CUDA if the stream reported an error, else GSR_OK.  The
+ * output of the call that gave up is unspecified; later calls are correct
+ * whether or not this function is called (the small-M kernel leaves its ticket
+ * counters at zero even when it gives up).  `code` (may be NULL) receives the raw
  * device error code, 0 if none: low byte = which wait gave up (1 producer
  * waiting for a free stage, 2 MMA issuer waiting for loaded data, 3 MMA issuer
  * waiting for a free accumulator, 4 epilogue waiting for a finished
@@ -202,6 +216,17 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
  * 0x300 = attention.
  */
 gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
+
+/*
+ * Releases the library's state for the (current device, stream) pair: the
+ * stream's 4-byte error word and, if a small-M call ran on it, its workspace.
+ * Waits for the stream first (queued kernels may still use them).  For callers
+ * that create and destroy streams: call it before destroying a stream the
+ * library was used on, from no other thread launching on that stream at the same
+ * time.  A later call on the stream allocates afresh.  GSR_OK if the pair holds
+ * nothing; GSR_ERR_CUDA if the wait or a free failed.
+ */
+gsr_status gsr_release_stream(struct CUstream_st* stream);
 
 /* Kernel the library would run for these sizes on the current device: 0 = tiled
  * (one CTA per 128-row tile), 1 = small-M, 2 = tiled on CTA pairs with 256 x 256
@@ -221,8 +246,10 @@ void gsr_set_path_override(int path);
 /* Raster grouping of the tiled kernels (process-wide): `group` consecutive tile rows
  * (M blocks) share each tile column before moving on, so that concurrently running
  * CTAs reuse the same A and B panels from L2 -- the "L2 swizzle" knob of the aikraft.ru
- * TileLang tutorial survey's "Knobs" section (3).  0 restores each kernel's default
- * (16 for one CTA per tile, 8 for CTA pairs).  For tuning and measurements. */
+ * TileLang tutorial survey's "Knobs" section (3).  0 restores the default, 16 row
+ * blocks per group (128-row blocks for one CTA per tile, 256-row blocks for CTA pairs).
+ * The small-M kernel walks K slabs, not a raster, and ignores it.  For tuning and
+ * measurements. */
 void gsr_set_raster_group(int group);
 
 /* Upper bound, in nanoseconds, on every wait inside the kernels (default 1 s).

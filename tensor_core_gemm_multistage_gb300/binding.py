@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_scale_relu_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, vp]
         L.gsr_device_status.restype = i32
         L.gsr_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        L.gsr_release_stream.restype = i32
+        L.gsr_release_stream.argtypes = [vp]
         L.gsr_select_path.restype = i32
         L.gsr_select_path.argtypes = [i64, i64, i64]
         L.gsr_set_path_override.restype = None
@@ -301,6 +303,17 @@ def gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, alpha: float, stream=None):
     if s != Status.OK:
         raise GsrError(s, "gemm_scale_relu_host")
     return hC
+
+
+def release_stream(stream=None, device=None):
+    """Frees the library's error word and small-M workspace of ``stream`` (after waiting
+    for it); a later call on the stream allocates afresh."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        s = lib().gsr_release_stream(_stream_handle(stream, dev) or None)
+    if s != Status.OK:
+        raise GsrError(s, "gsr_release_stream")
 
 
 def device_status(stream=None, device=None):

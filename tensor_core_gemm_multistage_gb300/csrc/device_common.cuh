@@ -48,6 +48,21 @@ struct Waiter {
         }
     }
 
+    // Teardown wait on a barrier a thread of the peer CTA arrives on (release at cluster
+    // scope): what that thread wrote before its arrive is visible after a true return.
+    __device__ __forceinline__ bool drain_cluster(uint32_t bar, uint32_t parity) const {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t spin = 1;; ++spin) {
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+            if ((spin & 63u) == 0u && globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1u;
+                atomicCAS(err, 0, kernel_code | kDevErrTeardown);
+                return false;
+            }
+        }
+    }
+
     __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
 };
 

@@ -52,13 +52,14 @@ struct PairCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
     static constexpr int OFF_C = OFF_B + STAGES * B_STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_C + C_BUFS * C_BUF_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    // full/empty per stage, two accumulator full/empty pairs, the MMA drain, the exit handshake
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM base, abort flag, peer's slots
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
     static constexpr uint32_t IDESC_HALF = idesc_f16_f32(BM, BN / 2, false, true);   // half-width units
     static constexpr uint32_t TEMPTY_ARRIVALS = 8;            // 4 epilogue warps x 2 CTAs
-    static constexpr uint64_t ABORT_GUARD_NS = 2000000;       // see the producer's exit
+    static constexpr uint32_t SLOT_DROPPED = 0x80000000u;     // handshake word: peer skipped slot 0
 
     static_assert(BN == 256 || BN == 128, "pair tile width");
     static_assert(STAGES >= 3, "pipeline depth");
@@ -104,8 +105,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     auto tfull_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * S + 4);
+    const uint32_t exit_bar = sb + Cfg::OFF_BAR + 8u * (2 * S + 5);    // leader's: peer's slot count
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 4);
+    volatile uint32_t* peer_slots = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -123,6 +126,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             mbar_init(tempty_bar(a), Cfg::TEMPTY_ARRIVALS);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(exit_bar, 1);                       // the peer producer's remote arrive
         *abort_flag = 0u;
         fence_mbarrier_init();
     }
@@ -147,13 +151,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         // columns (one 3-D box when B is described as 64-column chunks, else two 2-D boxes).
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_last();
+            const uint64_t pol_b = (p.test_flags & kTestBEvictFirst) ? l2_policy_evict_first()
+                                 : (p.test_flags & kTestBEvictNormal) ? l2_policy_evict_normal() : pol;
             uint32_t stage = 0, phase = 0;
-            uint32_t armed_mask = 0, armed_parity = 0;
-            bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+            uint32_t slots = 0;           // stage slots taken, in order: slot j is stage j % S
+            bool dropped0 = false;        // test hook: slot 0 was taken but never filled
+            bool drop_first = ((p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0) ||
+                              ((p.test_flags & kTestDropFirstLoadPeer) && blockIdx.x == 1);
             bool ok = true;
-            for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+            const bool serpentine = (p.test_flags & kTestKSerpentine) != 0;
+            uint32_t wave = 0;
+            for (int u = cluster; ok && u < p.num_units; u += nclusters, ++wave) {
                 int mb, nb, half;
                 pair_unit(u, p, mb, nb, half);
+                // odd waves walk K from the end (the MMA issuer takes stages as they come)
+                const bool backwards = serpentine && (wave & 1u);
                 // this CTA's B columns: half of the unit's width (128 or, for a half unit, 64)
                 const int cta_cols = half < 0 ? Cfg::HALF_N : Cfg::HALF_N / 2;
                 const int chunks = cta_cols / 64;
@@ -168,17 +180,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     }
                     if (drop_first) {
                         drop_first = false;   // test hook: this stage is never filled
+                        dropped0 = true;
                     } else {
                         const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
-                        if (rank == 0) {
-                            mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
-                            armed_mask |= 1u << stage;
-                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                        }
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
 #pragma unroll
                         for (int h = 0; h < Cfg::KSUB; ++h) {
                             // sub-block h: K columns [(KSUB kb + h) 64, +64); past K, TMA fills zeros
-                            const int k0 = (kb * Cfg::KSUB + h) * Cfg::BK;
+                            const int kbs = backwards ? n_stages - 1 - kb : kb;
+                            const int k0 = (kbs * Cfg::KSUB + h) * Cfg::BK;
                             tma_load_2d_pair(sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES + h * Cfg::A_SUB_BYTES,
                                              &tmA, leader_full, k0, m_row, pol);
                             const uint32_t b_dst = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES + h * Cfg::B_SUB_BYTES;
@@ -186,26 +196,63 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                 // boxes of b_box_chunks 64-column chunks (1 when half units exist)
                                 for (int j = 0; j < chunks; j += p.b_box_chunks)
                                     tma_load_3d_pair(b_dst + j * Cfg::B_CHUNK_BYTES, &tmB, leader_full, 0, k0,
-                                                     n_col / 64 + j, pol);
+                                                     n_col / 64 + j, pol_b);
                             } else {
                                 for (int j = 0; j < chunks; ++j)
                                     tma_load_2d_pair(b_dst + j * Cfg::B_CHUNK_BYTES, &tmB, leader_full,
-                                                     n_col + j * 64, k0, pol);
+                                                     n_col + j * 64, k0, pol_b);
                             }
                         }
                     }
+                    ++slots;
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
             }
-            // Leader: every stage it armed completes only once both CTAs' bytes landed.
-            for (int s = 0; s < S; ++s)
-                if (armed_mask & (1u << s)) w.drain(full_bar(s), (armed_parity >> s) & 1u);
-            // After an abort the peer cannot observe its own copies (they count on the
-            // leader's barrier); they depend on nothing and land within microseconds, so it
-            // waits a fixed guard time before it may leave.
-            if (!ok) {
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < Cfg::ABORT_GUARD_NS) {
+            // Exit handshake.  The peer's copies count on the leader's full barriers, so only
+            // the leader can see them land: the peer reports how many slots it took, and the
+            // leader settles every stage's last phase before the pair may leave (after an
+            // abort the two producers may have stopped at different slots).
+            if (rank == 1) {
+                st_shared_cluster_u32(map_to_cta(smem_u32((const void*)peer_slots), 0),
+                                      slots | (dropped0 ? Cfg::SLOT_DROPPED : 0u));
+                mbar_arrive_cluster(map_to_cta(exit_bar, 0));
+            } else if (w.drain_cluster(exit_bar, 0)) {
+                const uint32_t word = *peer_slots;
+                const uint32_t pslots = word & ~Cfg::SLOT_DROPPED;
+                const bool pdropped0 = (word & Cfg::SLOT_DROPPED) != 0;
+                const int n_stages = (p.num_k_blocks + Cfg::KSUB - 1) / Cfg::KSUB;
+                // one CTA's bytes of slot j (both CTAs' shares are equal): whole units stage
+                // HALF_N columns of B per CTA, half units half of that
+                auto share = [&](uint32_t j) -> uint32_t {
+                    const int u = cluster + (int)(j / (uint32_t)n_stages) * nclusters;
+                    const int chunks = (Cfg::BN == 256 && u >= p.num_full) ? Cfg::HALF_N / 128 : Cfg::HALF_N / 64;
+                    return (uint32_t)(Cfg::KSUB * (Cfg::A_SUB_BYTES + chunks * Cfg::B_CHUNK_BYTES));
+                };
+                // fills of stage s among the first n slots, less a skipped slot 0
+                auto fills = [&](uint32_t n, int s, bool skipped0) -> uint32_t {
+                    const uint32_t f = n > (uint32_t)s ? (n - 1u - (uint32_t)s) / (uint32_t)S + 1u : 0u;
+                    return f - ((s == 0 && skipped0) ? 1u : 0u);
+                };
+                for (int s = 0; s < S; ++s) {
+                    // phases [0, A) of full_bar(s) were armed by the leader, [0, P) received
+                    // the peer's copies; a slot is only taken once the one S slots earlier
+                    // has completed, so A and P differ by at most one.
+                    const uint32_t A = fills(slots, s, dropped0), P = fills(pslots, s, pdropped0);
+                    const uint32_t last = A > P ? A : P;
+                    if (last == 0) continue;
+                    if (P == A + 1) {
+                        // the peer filled a phase the leader never armed: arm it for the
+                        // peer's bytes alone (the phase before it has completed)
+                        mbar_arrive_expect_tx(full_bar(s), share(A * S + s));
+                    } else if (A == P + 1) {
+                        // the leader armed a phase the peer never filled: count the peer's
+                        // share as arrived, so the phase completes once the leader's bytes land
+                        mbar_complete_tx(full_bar(s), share(P * S + s));
+                    } else if (A != P) {
+                        atomicCAS(p.err, 0, kDevErrKernelTiled | kDevErrTeardown);
+                        continue;
+                    }
+                    w.drain(full_bar(s), (last - 1u) & 1u);
                 }
             }
         }
@@ -255,6 +302,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;
+        const bool store_first = (p.test_flags & kTestStoreEvictFirst) != 0;
+        const uint64_t pol_c = l2_policy_evict_first();
         uint32_t it = 0, cidx = 0;
         for (int u = cluster; u < p.num_units; u += nclusters, ++it) {
             const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
@@ -300,7 +349,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
                 if (et == 0) {
-                    tma_store_2d(&tmC, sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, n0 + c * 64, m0);
+                    if (store_first)
+                        tma_store_2d_hint(&tmC, sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, n0 + c * 64, m0, pol_c);
+                    else
+                        tma_store_2d(&tmC, sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, n0 + c * 64, m0);
                     bulk_commit_group();
                 }
                 ++cidx;

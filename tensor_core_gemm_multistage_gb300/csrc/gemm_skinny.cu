@@ -188,11 +188,26 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int nl = quad * 32 + lane;     // column of C inside the tile == TMEM lane
         const int et = threadIdx.x - 64;
         uint32_t it = 0;
+        bool live = true;
         for (int item = blockIdx.x; item < W; item += gridDim.x, ++it) {
             const int tile = item % n_tiles, slab = item / n_tiles;
             const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
-            const bool got = w.wait(tfull_bar(acc), acc_parity, kDevErrEpilogueFull);
-            if (!named_bar_and(1, 128, got)) break;
+            if (live) {
+                const bool got = w.wait(tfull_bar(acc), acc_parity, kDevErrEpilogueFull);
+                live = named_bar_and(1, 128, got);
+            }
+            if (!live) {
+                // This CTA gave up on a wait.  It still takes its ticket for each slab it was
+                // given, so that every tile's counter sees exactly S takers in this launch and
+                // ends it at 0 (the S-th taker resets it), whatever the other CTAs did: the
+                // next launch starts clean without the host having to intervene.  The tiles
+                // concerned are left unspecified (the timeout is reported).
+                if (S > 1 && et == 0) {
+                    const int old = atomicAdd(p.tickets + tile, 1);
+                    if (old + 1 == S) p.tickets[tile] = 0;
+                }
+                continue;
+            }
             tcgen05_fence_after();
 
             float v[MP];
@@ -341,27 +356,47 @@ size_t noalloc_scratch_need(int n_tiles, int slabs, int mp) {
     return 256 + tickets + slots * mp * 128 * sizeof(float);
 }
 
-cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tmAt, SkinnyParams p,
-                                  int mp, cudaStream_t stream) {
-    // Set-up, once per device and with that device current: the device address of the
-    // array.  (In host code the array's name is only a host-side stand-in.)
-    static std::mutex mu;
-    static void* base_of[kNoAllocMaxDevices] = {};
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_base[kNoAllocMaxDevices] = {};
+
+// Shared-memory attribute of one variant, set once per device (as launch_cfg does); under
+// CUDA's lazy loading this is also what places the kernel's code on the device.
+template <class Cfg>
+cudaError_t noalloc_prepare_cfg() {
+    return cudaFuncSetAttribute(gsr_skinny_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::SMEM_BYTES);
+}
+
+// Set-up, once per device and with that device current: the device address of the array (in
+// host code the array's name is only a host-side stand-in), and every kernel variant the
+// entry point can launch made resident, so that no later call makes the driver place
+// anything on the device.
+cudaError_t noalloc_base(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
-    void* base = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!base_of[dev]) {
-            void* ptr = nullptr;
-            e = cudaGetSymbolAddress(&ptr, g_gsr_noalloc_scratch);
-            if (e != cudaSuccess) return e;
-            base_of[dev] = ptr;
-        }
-        base = base_of[dev];
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+        void* ptr = nullptr;
+        if ((e = cudaGetSymbolAddress(&ptr, g_gsr_noalloc_scratch)) != cudaSuccess) return e;
+        if ((e = noalloc_prepare_cfg<Sk16>()) != cudaSuccess ||
+            (e = noalloc_prepare_cfg<Sk32>()) != cudaSuccess ||
+            (e = noalloc_prepare_cfg<Sk64>()) != cudaSuccess)
+            return e;
+        g_noalloc_base[dev] = ptr;
     }
+    *out = g_noalloc_base[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tmAt, SkinnyParams p,
+                                  int mp, cudaStream_t stream) {
+    void* base = nullptr;
+    cudaError_t e = noalloc_base(&base);
+    if (e != cudaSuccess) return e;
     if (noalloc_scratch_need(p.num_n_tiles, p.num_slabs, mp) > kNoAllocScratchBytes)
         return cudaErrorInvalidValue;
     unsigned char* b = static_cast<unsigned char*>(base);
@@ -375,6 +410,31 @@ cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tm
     if (mp == 32) return launch_cfg<Sk32>(tmBt, tmAt, p, stream);
     if (mp == 64) return launch_cfg<Sk64>(tmBt, tmAt, p, stream);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t noalloc_take_error(cudaStream_t stream, int* code) {
+    *code = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaSuccess;
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        base = g_noalloc_base[dev];
+    }
+    if (!base) return cudaSuccess;   // the entry point never ran on this device
+    int h = 0;
+    if ((e = cudaMemcpyAsync(&h, base, sizeof(int), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+        return e;
+    if (h != 0) {
+        if ((e = cudaMemsetAsync(base, 0, sizeof(int), stream)) != cudaSuccess ||
+            (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+            return e;
+    }
+    *code = h;
+    return cudaSuccess;
 }
 
 }  // namespace gsr

@@ -611,6 +611,13 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
     gsr_status s = validate(A, B, C, M, N, K, &nothing);
     if (s != GSR_OK || nothing) return s;
     if (M > kSkinnyMaxM) return GSR_ERR_INVALID_ARG;
+    const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    const int n_tiles = (int)((N + 127) / 128);
+    const int kbpt = (int)((K + 63) / 64);
+    // The tickets alone (every tile one slab) must fit whatever the device: checked before any
+    // CUDA call.  A K == 0 call needs no scratch.
+    if (K > 0 && gsr::noalloc_scratch_need(n_tiles, 1, mp) > gsr::noalloc_scratch_bytes())
+        return GSR_ERR_SCRATCH_LIMIT;
     int dev = 0, major = 0, minor = 0, sms = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
@@ -620,17 +627,14 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
         return cuda_fail(e);
     if (major != 10 || minor != 3) return GSR_ERR_UNSUPPORTED_DEVICE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-    const int n_tiles = (int)((N + 127) / 128);
-    const int kbpt = (int)((K + 63) / 64);
-    int S = 1, P = 1;
-    gsr::skinny_split(n_tiles, kbpt > 0 ? kbpt : 1, sms, &S, &P);
-    if (gsr::noalloc_scratch_need(n_tiles, S, mp) > gsr::noalloc_scratch_bytes())
-        return GSR_ERR_SCRATCH_LIMIT;
     if (K == 0) {
         e = cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
         return e == cudaSuccess ? GSR_OK : cuda_fail(e);
     }
+    int S = 1, P = 1;
+    gsr::skinny_split(n_tiles, kbpt, sms, &S, &P);
+    if (gsr::noalloc_scratch_need(n_tiles, S, mp) > gsr::noalloc_scratch_bytes())
+        return GSR_ERR_SCRATCH_LIMIT;
     if ((s = load_encoder()) != GSR_OK) return s;
     CUtensorMap tmBt, tmAt;
     if ((s = encode_fp16_2d(&tmBt, B, K, N, 64, 64)) != GSR_OK) return s;
@@ -649,7 +653,7 @@ gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_
     p.err = nullptr;
     p.C = static_cast<__half*>(C);
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
-    p.test_flags = 0;
+    p.test_flags = g_test_flags.load(std::memory_order_relaxed);
     p.epi = gsr::kEpiScaleRelu;
     p.bias = nullptr;
     e = gsr::launch_skinny_noalloc(tmBt, tmAt, p, mp, st);
@@ -721,23 +725,53 @@ gsr_status gsr_device_status(CUstream_st* stream, int* code) {
     if (e != cudaSuccess) return cuda_fail(e);
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    // the allocation-free entry point's error word (one per device; its calls run in order)
+    int h_fixed = 0;
+    if ((e = gsr::noalloc_take_error(st, &h_fixed)) != cudaSuccess) return cuda_fail(e);
+    StreamState s;
+    bool have = false;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_streams.find({dev, stream});
+        if (it != g_streams.end() && it->second.err) {
+            s = it->second;
+            have = true;
+        }
+    }
+    int h = 0;
+    if (have && (e = cudaMemcpy(&h, s.err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e);
+    if (h == 0) h = h_fixed;
+    if (code) *code = h;
+    if (h == 0) return GSR_OK;
+    if (have) {
+        if ((e = cudaMemset(s.err, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+        // The small-M kernel leaves its tickets at zero even when it gives up; clearing them
+        // here as well costs nothing and does not depend on it.
+        if (s.tickets && (e = cudaMemset(s.tickets, 0, s.ticket_count * sizeof(int))) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    return GSR_ERR_DEVICE_TIMEOUT;
+}
+
+gsr_status gsr_release_stream(CUstream_st* stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
     StreamState s;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_streams.find({dev, stream});
-        if (it == g_streams.end() || !it->second.err) return GSR_OK;
+        if (it == g_streams.end()) return GSR_OK;
         s = it->second;
+        g_streams.erase(it);
     }
-    int h = 0;
-    if ((e = cudaMemcpy(&h, s.err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
-        return cuda_fail(e);
-    if (code) *code = h;
-    if (h == 0) return GSR_OK;
-    // A launch that gave up may have left tickets half counted: start clean.
-    if ((e = cudaMemset(s.err, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e);
-    if (s.tickets && (e = cudaMemset(s.tickets, 0, s.ticket_count * sizeof(int))) != cudaSuccess)
-        return cuda_fail(e);
-    return GSR_ERR_DEVICE_TIMEOUT;
+    // Kernels queued earlier on the stream may still use the memory.
+    e = cudaStreamSynchronize(st);
+    cudaError_t e1 = cudaFree(s.err), e2 = cudaFree(s.partials), e3 = cudaFree(s.tickets);
+    if (e == cudaSuccess) e = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+    return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }
 
 int gsr_select_path(int64_t M, int64_t N, int64_t K) {

@@ -29,6 +29,11 @@ enum DeviceError : int {
 enum TestFlags : uint32_t {
     kTestDropFirstLoad = 1u,    // CTA 0's producer skips its first stage fill
     kTestNoChunkedB = 2u,       // host: copy B as separate 64-column boxes even when N % 64 == 0
+    kTestKSerpentine = 4u,      // pair kernel: every other wave of units walks K backwards
+    kTestStoreEvictFirst = 8u,  // pair kernel: C stores carry an L2 evict-first hint
+    kTestDropFirstLoadPeer = 16u,   // pair kernel: CTA 1 (the first pair's peer) skips its first fill
+    kTestBEvictFirst = 32u,     // pair kernel: B copies carry an L2 evict-first hint
+    kTestBEvictNormal = 64u,    // pair kernel: B copies carry an L2 evict-normal hint
 };
 
 // What the epilogue applies to the fp32 accumulator before the fp16 store.
@@ -128,6 +133,9 @@ cudaError_t launch_skinny_noalloc(const CUtensorMap& tmBt, const CUtensorMap& tm
                                   int mp, cudaStream_t stream);
 size_t noalloc_scratch_bytes();
 size_t noalloc_scratch_need(int n_tiles, int slabs, int mp);
+// Reads (after `stream`'s earlier work) and clears the error word of the fixed array on the
+// current device; *code = 0 when the allocation-free entry point never ran there.
+cudaError_t noalloc_take_error(cudaStream_t stream, int* code);
 
 // C[m, n] = GELU(bias[n]) for every m: the bias-GELU epilogue of an empty (K == 0) sum.
 cudaError_t launch_fill_bias_gelu(__half* C, const __half* bias, int M, int N, cudaStream_t stream);

@@ -158,3 +158,28 @@ def test_scale_entry_validates_like_the_fused_one():
     L = gsr.lib()
     assert L.gemm_scale(A, B, C, -1, 8, 8, ctypes.c_float(1.0), None) == gsr.Status.ERR_INVALID_ARG
     assert L.gemm_scale(A, B, A, 64, 64, 64, ctypes.c_float(1.0), None) == gsr.Status.ERR_ALIAS
+
+
+def test_noalloc_limits_are_checked_before_any_cuda_call():
+    # gemm_scale_relu_noalloc refuses M > 64 and sizes whose per-tile tickets alone exceed its
+    # fixed scratch array before it touches CUDA, so without a GPU these answer with the
+    # specific codes rather than GSR_ERR_CUDA.  The addresses are fake (A small, B 8 GiB at
+    # 64 GiB, C 64 GiB at 1 TiB: no overlaps), so this runs only where no GPU is present.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake device addresses: runs only where no GPU is present")
+    L = gsr.lib()
+    vp = ctypes.c_void_p
+    a, b, c = vp(0x10000), vp(1 << 36), vp(1 << 40)
+    one = ctypes.c_float(1.0)
+    assert L.gemm_scale_relu_noalloc(a, b, c, 64, 1 << 29, 8, one, None) == gsr.Status.ERR_SCRATCH_LIMIT
+    assert L.gemm_scale_relu_noalloc(a, b, c, 65, 64, 8, one, None) == gsr.Status.ERR_INVALID_ARG
+    # below the device-independent limit the call goes on to query the (absent) device
+    assert L.gemm_scale_relu_noalloc(a, b, c, 64, 1 << 20, 8, one, None) == gsr.Status.ERR_CUDA
+
+
+def test_release_stream_without_a_gpu_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert gsr.lib().gsr_release_stream(None) == gsr.Status.ERR_CUDA

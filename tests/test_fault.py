@@ -1,8 +1,8 @@
 """Failure detection without a GPU fault.
 
 Every wait inside the kernels is bounded.  A test-only flag makes the first CTA's TMA
-producer skip its first shared-memory fill, so that CTA's MMA issuer waits for data that
-never comes.  With a short limit the wait runs out, the kernel records a code in the
+producer (bit 0), or on the CTA-pair kernel the first pair's second CTA (bit 4), skip its
+first shared-memory fill, so the MMA issuer waits for data that never comes.  With a short limit the wait runs out, the kernel records a code in the
 stream's error word, drains what it started, frees its tensor memory and exits; the host
 reads GSR_ERR_DEVICE_TIMEOUT from gsr_device_status.  Nothing traps, and a normal call
 right after must still be correct (same context, small-M tickets reset).
@@ -28,19 +28,23 @@ def built():
     gsr.set_path_override(gsr.PATH_AUTO)
 
 
-@pytest.mark.parametrize("M,N,K,path,kernel", [(512, 1024, 1024, gsr.PATH_TILED, 0x100),
-                                               (1024, 2048, 1024, gsr.PATH_PAIR, 0x100),
-                                               (1024, 2048, 1024, gsr.PATH_PAIR_128, 0x100),
-                                               (300, 512, 1024, gsr.PATH_TILED_64, 0x100),
-                                               (16, 4096, 8192, gsr.PATH_SKINNY, 0x200)])
-def test_timeout_is_reported_and_the_gpu_stays_usable(M, N, K, path, kernel):
+@pytest.mark.parametrize("M,N,K,path,kernel,flags", [(512, 1024, 1024, gsr.PATH_TILED, 0x100, 1),
+                                                     (1024, 2048, 1024, gsr.PATH_PAIR, 0x100, 1),
+                                                     (1024, 2048, 1024, gsr.PATH_PAIR_128, 0x100, 1),
+                                                     # the first pair's second CTA skips its fill
+                                                     (1024, 2048, 1024, gsr.PATH_PAIR, 0x100, 16),
+                                                     (1024, 2048, 1024, gsr.PATH_PAIR_128, 0x100, 16),
+                                                     (2000, 3000, 1000, gsr.PATH_PAIR, 0x100, 16),
+                                                     (300, 512, 1024, gsr.PATH_TILED_64, 0x100, 1),
+                                                     (16, 4096, 8192, gsr.PATH_SKINNY, 0x200, 1)])
+def test_timeout_is_reported_and_the_gpu_stays_usable(M, N, K, path, kernel, flags):
     dev = torch.device("cuda", 0)
     A, B = make_inputs(M, N, K, seed=21)
     dA, dB = A.to(dev), B.to(dev)
     dC = torch.zeros(M, N, dtype=torch.float16, device=dev)
     gsr.set_path_override(path)
     gsr.set_wait_timeout_ns(50_000_000)        # 50 ms
-    gsr.set_test_flags(1)
+    gsr.set_test_flags(flags)
     try:
         gsr.gemm_scale_relu(dA, dB, dC, 0.5)
         status, code = gsr.device_status()
@@ -63,3 +67,54 @@ def test_timeout_is_reported_and_the_gpu_stays_usable(M, N, K, path, kernel):
     ref = oracle.gemm_scale_relu(A, B, 0.5).astype(np.float64)
     got = dC.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+
+
+def test_small_m_timeout_needs_no_status_call_to_recover():
+    # A small-M launch that gives up leaves its tile tickets at zero by itself: a caller that
+    # never reads gsr_device_status still gets correct results from the next call.
+    dev = torch.device("cuda", 0)
+    M, N, K = 16, 4096, 8192            # 32 tiles x 4 K slabs: every tile takes 4 tickets
+    A, B = make_inputs(M, N, K, seed=23, b_std_inv_sqrt_k=True)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.zeros(M, N, dtype=torch.float16, device=dev)
+    gsr.set_wait_timeout_ns(50_000_000)
+    gsr.set_test_flags(1)
+    try:
+        gsr.gemm_scale_relu(dA, dB, dC, 0.5)
+        torch.cuda.synchronize()
+    finally:
+        gsr.set_test_flags(0)
+        gsr.set_wait_timeout_ns(1_000_000_000)
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, return_pre=True)
+    ref = ref.astype(np.float64)
+    for _ in range(2):
+        dC.fill_(float("nan"))
+        gsr.gemm_scale_relu(dA, dB, dC, 0.5)
+        torch.cuda.synchronize()
+        got = dC.cpu().numpy().astype(np.float64)
+        assert not np.isnan(got).any()
+        assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+        assert np.all(got[z < -1e-2] == 0)
+    # the timeout is still on record for whoever asks
+    status, code = gsr.device_status()
+    assert status == gsr.Status.ERR_DEVICE_TIMEOUT and code & 0xF00 == 0x200
+    assert gsr.device_status() == (gsr.Status.OK, 0)
+
+
+def test_release_stream_frees_and_the_stream_stays_usable():
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream(dev)
+    M, N, K = 16, 2048, 4096
+    A, B = make_inputs(M, N, K, seed=29)
+    dA, dB = A.to(dev), B.to(dev)
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, return_pre=True)
+    for _ in range(2):                  # state allocated, released, allocated again
+        dC = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+        with torch.cuda.stream(s):
+            gsr.gemm_scale_relu(dA, dB, dC, 0.5, stream=s)
+        assert gsr.device_status(s) == (gsr.Status.OK, 0)
+        got = dC.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref.astype(np.float64)))
+        gsr.release_stream(s)
+        gsr.release_stream(s)           # nothing left: a no-op
+    assert gsr.device_status(s) == (gsr.Status.OK, 0)

@@ -182,6 +182,34 @@ def test_pair_kernel_half_width_tail(M, N, K, flags):
     check(C if rows is None else C[rows], ref, z, "half tail %dx%dx%d flags=%d" % (M, N, K, flags))
 
 
+_RASTER_REF = {}
+
+
+def _raster_reference(M, N, K):
+    if (M, N, K) not in _RASTER_REF:
+        A, B = make_inputs(M, N, K, seed=M + N + K + 1)
+        rows = None if M * N * K <= 2 ** 33 else sample_rows(M)
+        _RASTER_REF[(M, N, K)] = (A, B, rows) + oracle.gemm_scale_relu(A, B, 0.5, rows=rows,
+                                                                       return_pre=True)
+    return _RASTER_REF[(M, N, K)]
+
+
+@pytest.mark.parametrize("M,N,K", [(2000, 3000, 1000),   # pair: 96 tiles, the last 20 split; partial groups
+                                   (7600, 576, 264)])    # 30 row blocks of 256, 60 of 128: ragged groups
+@pytest.mark.parametrize("path", [gsr.PATH_TILED_256, gsr.PATH_TILED_128, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
+@pytest.mark.parametrize("group", [1, 3, 4, 16, 64])
+def test_raster_groups(M, N, K, path, group):
+    # gsr_set_raster_group changes which CTA computes which tile (the "L2 swizzle" knob); every
+    # grouping, including ones that leave the last group partial, must give the same result.
+    A, B, rows, ref, z = _raster_reference(M, N, K)
+    gsr.set_raster_group(group)
+    try:
+        C = run_gpu(A, B, 0.5, path)
+    finally:
+        gsr.set_raster_group(0)
+    check(C if rows is None else C[rows], ref, z, "raster %d path %d %dx%dx%d" % (group, path, M, N, K))
+
+
 def test_skinny_workload_through_tiled_path():
     w = WORKLOADS["skinny_decode"]
     parity(w.M, w.N, w.K, w.alpha, path=gsr.PATH_TILED, b_scaled=True)
