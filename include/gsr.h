@@ -260,7 +260,13 @@ void gsr_set_wait_timeout_ns(uint64_t ns);
 /* Test-only switches, 0 in normal use.  Bit 0: the first CTA's producer skips
  * its first shared-memory fill, so that CTA's waits run out (exercises the
  * bounded-wait path without faulting the GPU).  Bit 1: the tiled kernels copy B
- * as separate 64-column boxes even where one 3-D copy per stage would do. */
+ * as separate 64-column boxes even where one 3-D copy per stage would do.
+ * Bits 2-7 switch off or swap what the CTA-pair and attention kernels normally
+ * do, for measurements: bit 2 every wave of pair tiles walks K forward (no
+ * serpentine order); bit 3 C stores without the L2 evict-first hint; bit 4 the
+ * first pair's second CTA skips its first fill (like bit 0, on the other CTA);
+ * bit 5 / bit 6 B copies with an L2 evict-first / evict-normal hint instead of
+ * evict-last; bit 7 causal attention launches one head's query blocks at a time. */
 void gsr_set_test_flags(uint32_t flags);
 
 /* CUDA error code of the last failing CUDA call on this host thread (0: none). */

@@ -93,11 +93,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // CTA -> (query block, batch x head); the latest query blocks (most keys under a causal
-    // mask) are launched first
+    // CTA -> (query block, batch x head).  The (batch x head) slices are taken in groups of
+    // head_group; within a group the latest query blocks of all its heads (the most keys under
+    // a causal mask) are launched first, then the ones before them, so the blocks launched last
+    // are the shortest and the GPU drains evenly, while the group's K and V stay in L2.
+    // head_group = 1 walks one head's query blocks at a time, latest first.
     const int n_qb = (p.Sq + NQ * Cfg::BQ - 1) / (NQ * Cfg::BQ);
-    const int qb = n_qb - 1 - (int)(blockIdx.x % n_qb);
-    const int bh = blockIdx.x / n_qb;
+    const int per_group = p.head_group * n_qb;
+    const int grp = (int)blockIdx.x / per_group;
+    const int r_in = (int)blockIdx.x - grp * per_group;
+    const int gsz = min(p.BH - grp * p.head_group, p.head_group);   // the last group may be smaller
+    const int qb = n_qb - 1 - r_in / gsz;
+    const int bh = grp * p.head_group + r_in % gsz;
     const int q_base = qb * NQ * Cfg::BQ;
     // key tiles each query tile needs (causal: keys k <= q + offset only); nkv[0] <= nkv[1]
     int nkv[NQ];

@@ -1,4 +1,5 @@
-// device_common.cuh - bounded mbarrier waits shared by the kernels.
+// device_common.cuh - bounded mbarrier waits, the raster order of the tiled kernels, and the
+// epilogue arithmetic, shared by the kernels.
 //
 // Every wait in the kernels is bounded: after `timeout_ns` of %globaltimer time the
 // waiting thread records an error code in the per-device error word, raises the CTA's
@@ -67,6 +68,23 @@ struct Waiter {
 };
 
 // ---------------------------------------------------------------------------
+// Tile scheduling shared by the one-CTA and CTA-pair tiled kernels
+// ---------------------------------------------------------------------------
+// Tile t -> (m block, n block), grouped along M: `group_m` consecutive M blocks share each
+// N block before the walk moves to the next N block (the last group may be shorter), so
+// the tiles running at one time reuse the same A panels (and each B panel) from L2.
+__device__ __forceinline__ void raster_tile_coords(int t, int num_m_blocks, int num_n_blocks,
+                                                   int group_m, int& mb, int& nb) {
+    const int per_group = group_m * num_n_blocks;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int gsz = min(num_m_blocks - first_m, group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % gsz;
+    nb = r / gsz;
+}
+
+// ---------------------------------------------------------------------------
 // Epilogue functions on the fp32 accumulator
 // ---------------------------------------------------------------------------
 // GELU, tanh approximation: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3).
@@ -126,6 +144,37 @@ __device__ __forceinline__ uint4 epilogue_8(const uint32_t* src, float alpha, in
     v.z = out[2];
     v.w = out[3];
     return v;
+}
+
+// One 64-column chunk of a 128-row output tile, from the four epilogue warps' registers (thread
+// = tile row `row`, r0/r1 = the chunk's two 32-column halves of fp32 accumulators) to C: wait
+// until the previous store from staging buffer `buf` has read it, write the row's 64 outputs
+// into the buffer in the 128-byte-swizzled layout of the tensor map (16-byte chunk j of row r
+// at j ^ (r & 7): conflict-free), and hand the buffer to one TMA store of the box at (col0, m0),
+// which clips whatever lies outside C.  Named barrier 1 spans the 128 epilogue threads; `et`
+// is the thread's index among them.  `pol`, when `hinted`, is the L2 policy of the written lines.
+__device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                                     uint8_t* buf, uint32_t buf_saddr, int row, int et,
+                                                     const TiledParams& p, int col0, int m0,
+                                                     const CUtensorMap* tmC, bool hinted, uint64_t pol) {
+    if (et == 0) bulk_wait_group_read<1>();   // the store from this buffer is done reading it
+    named_bar_sync(1, 128);
+    uint8_t* crow = buf + row * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t* src = (j < 4) ? (r0 + 8 * j) : (r1 + 8 * (j - 4));
+        const uint4 v = epilogue_8(src, p.alpha, p.epi, p.bias, col0 + 8 * j, p.N);
+        *reinterpret_cast<uint4*>(crow + ((j ^ (row & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (et == 0) {
+        if (hinted)
+            tma_store_2d_hint(tmC, buf_saddr, col0, m0, pol);
+        else
+            tma_store_2d(tmC, buf_saddr, col0, m0);
+        bulk_commit_group();
+    }
 }
 
 }  // namespace gsr

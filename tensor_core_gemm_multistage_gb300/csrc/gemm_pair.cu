@@ -66,17 +66,6 @@ struct PairCfg {
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
 };
 
-__device__ __forceinline__ void pair_tile_coords(int t, int num_m_blocks, int num_n_blocks,
-                                                 int group_m, int& mb, int& nb) {
-    const int per_group = group_m * num_n_blocks;
-    const int g = t / per_group;
-    const int first_m = g * group_m;
-    const int gsz = min(num_m_blocks - first_m, group_m);
-    const int r = t - g * per_group;
-    mb = first_m + r % gsz;
-    nb = r / gsz;
-}
-
 // Work unit u -> tile (mb, nb) and which half of its columns (-1: the whole tile).  Units
 // below num_full are whole tiles; each later tile is split into two half-width units.
 __device__ __forceinline__ void pair_unit(int u, const TiledParams& p, int& mb, int& nb, int& half) {
@@ -87,7 +76,7 @@ __device__ __forceinline__ void pair_unit(int u, const TiledParams& p, int& mb, 
         t = p.num_full + (v >> 1);
         half = v & 1;
     }
-    pair_tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+    raster_tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
 }
 
 template <class Cfg>
@@ -159,12 +148,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             bool drop_first = ((p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0) ||
                               ((p.test_flags & kTestDropFirstLoadPeer) && blockIdx.x == 1);
             bool ok = true;
-            const bool serpentine = (p.test_flags & kTestKSerpentine) != 0;
+            // Serpentine K order: odd waves of units walk K from the end.  A wave's tiles share
+            // their A panels with the next wave's (same raster group); read forward twice, the
+            // panels (4 MiB each at K = 8192) are gone from L2 before the next wave reaches
+            // them, while read back to front the next wave starts on the k-blocks the last one
+            // touched most recently (8192^3: DRAM reads 1283 -> 819 MB per launch).  The MMA
+            // issuer takes the stages as they come; only the summation order changes.
+            const bool serpentine = (p.test_flags & kTestKForward) == 0;
             uint32_t wave = 0;
             for (int u = cluster; ok && u < p.num_units; u += nclusters, ++wave) {
                 int mb, nb, half;
                 pair_unit(u, p, mb, nb, half);
-                // odd waves walk K from the end (the MMA issuer takes stages as they come)
                 const bool backwards = serpentine && (wave & 1u);
                 // this CTA's B columns: half of the unit's width (128 or, for a half unit, 64)
                 const int cta_cols = half < 0 ? Cfg::HALF_N : Cfg::HALF_N / 2;
@@ -302,7 +296,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;
-        const bool store_first = (p.test_flags & kTestStoreEvictFirst) != 0;
+        // C is written once and never read here: its lines go first when L2 needs room, so
+        // they do not push out A and B panels still in use
+        const bool store_first = (p.test_flags & kTestStoreNoHint) == 0;
         const uint64_t pol_c = l2_policy_evict_first();
         uint32_t it = 0, cidx = 0;
         for (int u = cluster; u < p.num_units; u += nclusters, ++it) {
@@ -337,24 +333,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     if (lane == 0) mbar_arrive_cluster(leader_tempty);
                 }
                 const uint32_t buf = cidx & 1u;
-                if (et == 0) bulk_wait_group_read<1>();
-                named_bar_sync(1, 128);
-                uint8_t* crow = smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES + row * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t* src = (j < 4) ? (r0 + 8 * j) : (r1 + 8 * (j - 4));
-                    const uint4 v = epilogue_8(src, p.alpha, p.epi, p.bias, n0 + c * 64 + 8 * j, p.N);
-                    *reinterpret_cast<uint4*>(crow + ((j ^ (row & 7)) << 4)) = v;
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (et == 0) {
-                    if (store_first)
-                        tma_store_2d_hint(&tmC, sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, n0 + c * 64, m0, pol_c);
-                    else
-                        tma_store_2d(&tmC, sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, n0 + c * 64, m0);
-                    bulk_commit_group();
-                }
+                epilogue_store_chunk(r0, r1, smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES,
+                                     sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, row, et, p, n0 + c * 64, m0,
+                                     &tmC, store_first, pol_c);
                 ++cidx;
             }
         }

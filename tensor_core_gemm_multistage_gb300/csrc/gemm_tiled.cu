@@ -55,19 +55,6 @@ struct TiledCfg {
     static_assert(BN % 64 == 0 && BN <= 256, "BN must be a multiple of 64, at most 256");
 };
 
-// Tile t -> (m block, n block), grouped along M: `group_m` consecutive M blocks share each
-// N block before moving to the next N block.
-__device__ __forceinline__ void tile_coords(int t, int num_m_blocks, int num_n_blocks, int group_m,
-                                            int& mb, int& nb) {
-    const int per_group = group_m * num_n_blocks;
-    const int g = t / per_group;
-    const int first_m = g * group_m;
-    const int gsz = min(num_m_blocks - first_m, group_m);
-    const int r = t - g * per_group;
-    mb = first_m + r % gsz;
-    nb = r / gsz;
-}
-
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gsr_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -128,7 +115,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 int mb, nb;
-                tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+                raster_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
                         ok = false;
@@ -218,7 +205,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (!named_bar_and(1, 128, got)) break;
             tcgen05_fence_after();
             int mb, nb;
-            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+            raster_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
             const int m0 = mb * Cfg::BM, n0 = nb * Cfg::BN;
             const int nchunks = (min(Cfg::BN, p.N - n0) + 63) / 64;   // skip columns past N
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * Cfg::BN;
@@ -233,22 +220,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     mbar_arrive(tempty_bar(acc));   // MMA may now overwrite this accumulator
                 }
                 const uint32_t buf = cidx & 1u;
-                if (et == 0) bulk_wait_group_read<1>();   // the store from this buffer is done reading
-                named_bar_sync(1, 128);
-                uint8_t* crow = smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES + row * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t* src = (j < 4) ? (r0 + 8 * j) : (r1 + 8 * (j - 4));
-                    const uint4 v = epilogue_8(src, p.alpha, p.epi, p.bias, n0 + c * 64 + 8 * j, p.N);
-                    // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7).
-                    *reinterpret_cast<uint4*>(crow + ((j ^ (row & 7)) << 4)) = v;
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (et == 0) {
-                    tma_store_2d(&tmC, sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, n0 + c * 64, m0);
-                    bulk_commit_group();
-                }
+                epilogue_store_chunk(r0, r1, smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES,
+                                     sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, row, et, p, n0 + c * 64, m0,
+                                     &tmC, false, 0);
                 ++cidx;
             }
         }

@@ -709,6 +709,18 @@ gsr_status flash_attention_fwd(const void* Q, const void* K, const void* V, void
     p.causal = causal ? 1 : 0;
     p.causal_offset = (int)(seq_kv - seq_q);
     p.scale_log2 = (float)(scale * 1.4426950408889634);
+    // Causal blocks differ in length (the latest query blocks see the most keys): launch them
+    // longest first across as many heads as keep their K and V (seq_kv x head_dim x 4 bytes
+    // each) within ~48 MiB of L2; without a mask every block is equally long and one head's
+    // blocks run together.
+    {
+        const uint64_t kv_head = (uint64_t)seq_kv * (uint64_t)head_dim * 4u;
+        const bool head_major = (g_test_flags.load(std::memory_order_relaxed) & gsr::kTestAttnHeadMajor) != 0;
+        uint64_t g = (causal && !head_major) ? ((uint64_t)48 << 20) / (kv_head ? kv_head : 1) : 1;
+        if (g < 1) g = 1;
+        if (g > (uint64_t)BH) g = (uint64_t)BH;
+        p.head_group = (int)g;
+    }
     p.O = static_cast<__half*>(O);
     p.lse = lse;
     p.err = ss.err;

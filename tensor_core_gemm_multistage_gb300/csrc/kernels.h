@@ -29,11 +29,12 @@ enum DeviceError : int {
 enum TestFlags : uint32_t {
     kTestDropFirstLoad = 1u,    // CTA 0's producer skips its first stage fill
     kTestNoChunkedB = 2u,       // host: copy B as separate 64-column boxes even when N % 64 == 0
-    kTestKSerpentine = 4u,      // pair kernel: every other wave of units walks K backwards
-    kTestStoreEvictFirst = 8u,  // pair kernel: C stores carry an L2 evict-first hint
+    kTestKForward = 4u,         // pair kernel: every wave walks K forward (no serpentine order)
+    kTestStoreNoHint = 8u,      // pair kernel: C stores without the L2 evict-first hint
     kTestDropFirstLoadPeer = 16u,   // pair kernel: CTA 1 (the first pair's peer) skips its first fill
-    kTestBEvictFirst = 32u,     // pair kernel: B copies carry an L2 evict-first hint
-    kTestBEvictNormal = 64u,    // pair kernel: B copies carry an L2 evict-normal hint
+    kTestBEvictFirst = 32u,     // pair kernel: B copies with an L2 evict-first hint (not evict-last)
+    kTestBEvictNormal = 64u,    // pair kernel: B copies with an L2 evict-normal hint
+    kTestAttnHeadMajor = 128u,  // attention: one head's query blocks at a time, even when causal
 };
 
 // What the epilogue applies to the fp32 accumulator before the fp16 store.
@@ -95,6 +96,7 @@ struct AttnParams {
     int causal;             // keep key k for query q when k <= q + causal_offset
     int causal_offset;      // Skv - Sq
     float scale_log2;       // softmax scale * log2(e)
+    int head_group;         // launch order: query blocks longest first within groups of this many heads
     __half* O;              // (BH, Sq, D) row-major
     float* lse;             // optional (BH, Sq): natural-log log-sum-exp of the scaled scores
     int* err;

@@ -9,6 +9,9 @@ static_assert), so the runtime knobs are:
   kernel   tiled 128x256, 128x128 or 128x64, CTA pair 256x256 or 256x128, small-M (M <= 64)
   raster   the grouping of tile rows for L2 reuse (gsr_set_raster_group)
   b_copy   3-D copies for B, or separate 64-column 2-D boxes (CTA-pair kernels, N % 64 == 0)
+  l2       the CTA-pair kernels' L2 handling: "default" (serpentine K order across waves,
+           evict-last A and B, evict-first C stores), "k_forward" (every wave walks K forward),
+           "b_evict_first" (B copies marked evict-first)
 
     python -m tensor_core_gemm_multistage_gb300.sweep --M 8192 --N 8192 --K 8192
 
@@ -31,6 +34,7 @@ KERNELS = {"tiled_128x256": gsr.PATH_TILED_256, "tiled_128x128": gsr.PATH_TILED_
            "pair_256x256": gsr.PATH_PAIR, "pair_256x128": gsr.PATH_PAIR_128, "small_m": gsr.PATH_SKINNY}
 RASTERS = (0, 4, 16)     # 0: the kernel's default grouping
 NO_3D_B = 2              # test flag bit 1
+L2_MODES = {"default": 0, "k_forward": 4, "b_evict_first": 32}   # test flag bits 2 and 5
 
 
 def candidates(M: int, N: int, K: int):
@@ -41,9 +45,11 @@ def candidates(M: int, N: int, K: int):
             continue
         rasters = (0,) if name == "small_m" else RASTERS
         copies = ("3d", "2d") if (name.startswith("pair_") and N % 64 == 0) else ("default",)
+        l2s = tuple(L2_MODES) if name.startswith("pair_") else ("default",)
         for r in rasters:
             for c in copies:
-                out.append({"kernel": name, "path": path, "raster": r, "b_copy": c})
+                for l2 in l2s:
+                    out.append({"kernel": name, "path": path, "raster": r, "b_copy": c, "l2": l2})
     return out
 
 
@@ -51,7 +57,7 @@ def time_config(cfg, A, B, C, alpha, warmup=5, iters=30):
     import torch
     gsr.set_path_override(cfg["path"])
     gsr.set_raster_group(cfg["raster"])
-    gsr.set_test_flags(NO_3D_B if cfg["b_copy"] == "2d" else 0)
+    gsr.set_test_flags((NO_3D_B if cfg["b_copy"] == "2d" else 0) | L2_MODES[cfg.get("l2", "default")])
     try:
         for _ in range(warmup):
             gsr.gemm_scale_relu(A, B, C, alpha)

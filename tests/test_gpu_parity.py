@@ -365,3 +365,17 @@ def test_gpu_validation_codes():
         == gsr.Status.ERR_ALIAS
     assert gsr.gemm_scale_relu_ptr(dA.data_ptr() + 2, dB.data_ptr(), dB.data_ptr(), 8, 8, 8, 1.0) \
         == gsr.Status.ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("flags", [4, 8, 32, 64, 4 | 32])
+def test_pair_kernel_l2_switches(flags):
+    # The pair kernel walks K backwards in every other wave of tiles by default; bit 2 walks
+    # it forward everywhere, bit 3 drops the evict-first hint of the C stores, bits 5/6 change
+    # the L2 hint of the B copies.  4096 x 4096 x 1024 has three and a half waves of tiles.
+    A, B, rows, ref, z = _raster_reference(4096, 4096, 1024)
+    gsr.set_test_flags(flags)
+    try:
+        C = run_gpu(A, B, 0.5, gsr.PATH_PAIR)
+    finally:
+        gsr.set_test_flags(0)
+    check(C if rows is None else C[rows], ref, z, "pair flags %d" % flags)

@@ -12,6 +12,8 @@ def test_candidates_respect_each_kernels_limits():
                        "pair_256x128"}   # no small-M at M > 64
     assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x256"} == {"3d", "2d"}
     assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x128"} == {"3d", "2d"}
+    assert {c["l2"] for c in big if c["kernel"] == "pair_256x256"} == set(sweep.L2_MODES)
+    assert {c["l2"] for c in big if c["kernel"].startswith("tiled")} == {"default"}
     small = sweep.candidates(16, 1000, 4096)                                    # N % 64 != 0
     assert "small_m" in {c["kernel"] for c in small}
     assert {c["b_copy"] for c in small} == {"default"}
