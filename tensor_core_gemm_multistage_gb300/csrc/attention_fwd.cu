@@ -48,7 +48,7 @@ struct AttnCfg {
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
-    static constexpr int NUM_BARS = 12;
+    static constexpr int NUM_BARS = 17;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     // no alignment slack: the window is declared 1024-byte aligned and the kernel checks it
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -80,47 +80,61 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint8_t* smem = smem_raw;
     const uint32_t sb = smem_u32(smem);
 
-    // barriers: 0 qfull | 1+s full | 3+s empty | 5+q sfull | 7+q pfull | 9+q odone | 11 drain
+    // barriers: 0 qfull | 1 qfree | 2+s full | 4+s empty | 6+q sfull | 8+q pfull | 10+q odone |
+    // 12+i item published | 14+i item read | 16 drain
     auto bar = [&](int i) { return sb + Cfg::OFF_BAR + 8u * i; };
-    const uint32_t qfull = bar(0), drain = bar(11);
-    auto full = [&](int s) { return bar(1 + s); };
-    auto empty = [&](int s) { return bar(3 + s); };
-    auto sfull = [&](int q) { return bar(5 + q); };
-    auto pfull = [&](int q) { return bar(7 + q); };
-    auto odone = [&](int q) { return bar(9 + q); };
+    const uint32_t qfull = bar(0), qfree = bar(1), drain = bar(16);
+    auto full = [&](int s) { return bar(2 + s); };
+    auto empty = [&](int s) { return bar(4 + s); };
+    auto sfull = [&](int q) { return bar(6 + q); };
+    auto pfull = [&](int q) { return bar(8 + q); };
+    auto odone = [&](int q) { return bar(10 + q); };
+    auto item_pub = [&](int i) { return bar(12 + i); };
+    auto item_read = [&](int i) { return bar(14 + i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC + 4);
+    volatile int* item_box = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 8);   // 2 slots
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // CTA -> (query block, batch x head).  The (batch x head) slices are taken in groups of
-    // head_group; within a group the latest query blocks of all its heads (the most keys under
-    // a causal mask) are launched first, then the ones before them, so the blocks launched last
-    // are the shortest and the GPU drains evenly, while the group's K and V stay in L2.
-    // head_group = 1 walks one head's query blocks at a time, latest first.
     const int n_qb = (p.Sq + NQ * Cfg::BQ - 1) / (NQ * Cfg::BQ);
-    const int per_group = p.head_group * n_qb;
-    const int grp = (int)blockIdx.x / per_group;
-    const int r_in = (int)blockIdx.x - grp * per_group;
-    const int gsz = min(p.BH - grp * p.head_group, p.head_group);   // the last group may be smaller
-    const int qb = n_qb - 1 - r_in / gsz;
-    const int bh = grp * p.head_group + r_in % gsz;
-    const int q_base = qb * NQ * Cfg::BQ;
-    // key tiles each query tile needs (causal: keys k <= q + offset only); nkv[0] <= nkv[1]
-    int nkv[NQ];
+
+    // Work item -> (query block, batch x head) and the key tiles each query tile needs.  The
+    // (batch x head) slices are taken in groups of head_group; within a group the latest query
+    // blocks of all its heads (the most keys under a causal mask) come first, then the ones
+    // before them, so the items fetched last are the shortest and the CTAs drain together,
+    // while the group's K and V stay in L2.  head_group = 1 walks one head at a time.
+    struct Item {
+        int bh, q_base, nkv[NQ], nkv_max;
+    };
+    auto decode = [&](int item) {
+        Item it;
+        const int per_group = p.head_group * n_qb;
+        const int grp = item / per_group;
+        const int r_in = item - grp * per_group;
+        const int gsz = min(p.BH - grp * p.head_group, p.head_group);   // the last group may be smaller
+        const int qb = n_qb - 1 - r_in / gsz;
+        it.bh = grp * p.head_group + r_in % gsz;
+        it.q_base = qb * NQ * Cfg::BQ;
+        // key tiles each query tile needs (causal: keys k <= q + offset only); nkv[0] <= nkv[1]
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        int kv_end = p.Skv;
-        if (p.causal) kv_end = min(p.Skv, q_base + (q + 1) * Cfg::BQ + p.causal_offset);
-        nkv[q] = kv_end > 0 ? (kv_end + Cfg::BKV - 1) / Cfg::BKV : 0;
-    }
-    const int nkv_max = nkv[NQ - 1];
+        for (int q = 0; q < NQ; ++q) {
+            int kv_end = p.Skv;
+            if (p.causal) kv_end = min(p.Skv, it.q_base + (q + 1) * Cfg::BQ + p.causal_offset);
+            it.nkv[q] = kv_end > 0 ? (kv_end + Cfg::BKV - 1) / Cfg::BKV : 0;
+        }
+        it.nkv_max = it.nkv[NQ - 1];
+        return it;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(qfull, 1);
+        mbar_init(qfree, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
+            mbar_init(item_pub(s), 1);
+            mbar_init(item_read(s), 1 + Cfg::SM_THREADS / 32);   // the MMA lane and every softmax warp
         }
         for (int q = 0; q < NQ; ++q) {
             mbar_init(sfull(q), 1);
@@ -147,106 +161,166 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const Waiter w{p.err, p.timeout_ns, abort_flag, kDevErrKernelAttention};
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && nkv_max > 0) {
+        // ------------------------------------------------------------ work fetch + TMA producer
+        // Takes the next work item from the launch's counter and publishes it to the other roles
+        // (a 2-slot box, so it can run one item ahead), then loads the item's Q tiles (once the
+        // previous item's last Q K^T products have read theirs) and its ring entries, which
+        // continue from the previous item's: entry e of an item holds K_e and V_{e-1}.
+        if (lane == 0) {
             const uint64_t pol = l2_policy_evict_last();   // K and V are read by every query block
-            uint32_t armed = 0, armed_parity = 0;          // bit 0 Q, bits 1-2 ring entries
-            const bool drop_q = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
-            if (!drop_q) {
-                mbar_arrive_expect_tx(qfull, NQ * Cfg::Q_BYTES);
+            uint32_t n_pub = 0, n_q = 0, g = 0;            // items published, Q loads, ring entries
+            bool q_armed = false;
+            uint32_t ring_armed = 0, ring_parity = 0;
+            bool drop_q = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
+            while (true) {
+                int item = atomicAdd(p.work, 1);
+                if (item >= p.num_items) item = -1;
+                const uint32_t box = n_pub & 1u;
+                // the box's previous item has been read by every role
+                if (!w.wait(item_read(box), ((n_pub >> 1) & 1u) ^ 1u, kDevErrProducerEmpty)) break;
+                item_box[box] = item;
+                mbar_arrive(item_pub(box));          // release: the consumers read the box after
+                ++n_pub;
+                if (item < 0) break;
+                const Item it = decode(item);
+                if (it.nkv_max == 0) continue;       // no keys: O = 0 needs no copies
+                if (n_q > 0 && !w.wait(qfree, (n_q - 1) & 1u, kDevErrProducerEmpty)) break;
+                if (drop_q) {
+                    drop_q = false;                  // test hook: this Q is never loaded
+                } else {
+                    mbar_arrive_expect_tx(qfull, NQ * Cfg::Q_BYTES);
 #pragma unroll
-                for (int q = 0; q < NQ; ++q)
+                    for (int q = 0; q < NQ; ++q)
 #pragma unroll
-                    for (int c = 0; c < Cfg::DCH; ++c)
-                        tma_load_3d(sb + Cfg::OFF_Q + q * Cfg::Q_BYTES + c * Cfg::CHUNK_BYTES, &tmQ, qfull,
-                                    c * 64, q_base + q * Cfg::BQ, bh, pol);
-                armed |= 1u;
+                        for (int c = 0; c < Cfg::DCH; ++c)
+                            tma_load_3d(sb + Cfg::OFF_Q + q * Cfg::Q_BYTES + c * Cfg::CHUNK_BYTES, &tmQ, qfull,
+                                        c * 64, it.q_base + q * Cfg::BQ, it.bh, pol);
+                    q_armed = true;
+                }
+                ++n_q;
+                bool ok = true;
+                // entry e: K_e (e < nkv_max) and V_{e-1} (e >= 1); the last entry holds only V
+                for (int e = 0; e <= it.nkv_max; ++e, ++g) {
+                    const int s = (int)(g & 1u);
+                    const uint32_t ph = (g >> 1) & 1u;
+                    if (!w.wait(empty(s), ph ^ 1u, kDevErrProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool has_k = e < it.nkv_max, has_v = e >= 1;
+                    mbar_arrive_expect_tx(full(s), (has_k ? Cfg::KV_BYTES : 0) + (has_v ? Cfg::KV_BYTES : 0));
+                    if (has_k) {
+#pragma unroll
+                        for (int c = 0; c < Cfg::DCH; ++c)
+                            tma_load_3d(sb + Cfg::OFF_K + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmK, full(s),
+                                        c * 64, e * Cfg::BKV, it.bh, pol);
+                    }
+                    if (has_v) {
+#pragma unroll
+                        for (int c = 0; c < Cfg::DCH; ++c)
+                            tma_load_3d(sb + Cfg::OFF_V + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmV, full(s),
+                                        c * 64, (e - 1) * Cfg::BKV, it.bh, pol);
+                    }
+                    ring_armed |= 1u << s;
+                    ring_parity = (ring_parity & ~(1u << s)) | (ph << s);
+                }
+                if (!ok) break;
             }
-            // entry e: K_e (e < nkv_max) and V_{e-1} (e >= 1); the last entry holds only V
-            for (int e = 0; e <= nkv_max; ++e) {
-                const int s = e & 1;
-                const uint32_t ph = (e >> 1) & 1u;
-                if (!w.wait(empty(s), ph ^ 1u, kDevErrProducerEmpty)) break;
-                const bool has_k = e < nkv_max, has_v = e >= 1;
-                mbar_arrive_expect_tx(full(s), (has_k ? Cfg::KV_BYTES : 0) + (has_v ? Cfg::KV_BYTES : 0));
-                if (has_k) {
-#pragma unroll
-                    for (int c = 0; c < Cfg::DCH; ++c)
-                        tma_load_3d(sb + Cfg::OFF_K + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmK, full(s),
-                                    c * 64, e * Cfg::BKV, bh, pol);
-                }
-                if (has_v) {
-#pragma unroll
-                    for (int c = 0; c < Cfg::DCH; ++c)
-                        tma_load_3d(sb + Cfg::OFF_V + s * Cfg::KV_BYTES + c * Cfg::CHUNK_BYTES, &tmV, full(s),
-                                    c * 64, (e - 1) * Cfg::BKV, bh, pol);
-                }
-                armed |= 2u << s;
-                armed_parity = (armed_parity & ~(2u << s)) | (ph << (1 + s));
+            // The launch's fetch counter: this CTA takes no more items.  The last CTA to get here
+            // (after every other one has taken its last item) resets the counter for the next
+            // launch on the stream.
+            __threadfence();
+            if (atomicAdd(p.work + 1, 1) == (int)gridDim.x - 1) {
+                atomicExch(p.work, 0);
+                atomicExch(p.work + 1, 0);
             }
             // every copy started must land before the CTA may exit
-            if (armed & 1u) w.drain(qfull, 0);
+            if (q_armed) w.drain(qfull, (n_q - 1) & 1u);
             for (int s = 0; s < 2; ++s)
-                if (armed & (2u << s)) w.drain(full(s), (armed_parity >> (1 + s)) & 1u);
+                if (ring_armed & (1u << s)) w.drain(full(s), (ring_parity >> s) & 1u);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && nkv_max > 0) {
-            // PV_q(t) = P_q(t) V_t accumulated into O_q; V_t sits in ring entry t + 1, which
-            // the caller has waited for and frees after the step.  After its last key tile,
-            // O_q is published to the softmax group.
-            auto issue_pv = [&](int q, int t) -> bool {
-                const int s = (t + 1) & 1;
-                if (!w.wait(pfull(q), t & 1, kDevErrMmaFull)) return false;
+        if (lane == 0) {
+            uint32_t n_item = 0, n_q = 0, g = 0;      // items taken, items with keys, ring entries
+            uint32_t pv_n0 = 0u, pv_n1 = 0u;          // pfull phases waited for, per query tile
+            bool ok = true;
+            while (ok) {
+                const uint32_t box = n_item & 1u;
+                if (!w.wait(item_pub(box), (n_item >> 1) & 1u, kDevErrMmaFull)) break;
+                const int item = item_box[box];
+                mbar_arrive(item_read(box));
+                ++n_item;
+                if (item < 0) break;
+                const Item it = decode(item);
+                if (it.nkv_max == 0) continue;
+                if (!w.wait(qfull, n_q & 1u, kDevErrMmaFull)) break;
+                ++n_q;
                 tcgen05_fence_after();
-                const uint32_t v_s = sb + Cfg::OFF_V + s * Cfg::KV_BYTES;
-                const uint32_t p_t = tmem_base + Cfg::T_S + q * 128 + Cfg::P_COL;
+                // PV_q(t) = P_q(t) V_t accumulated into O_q; V_t sits in the ring slot `s` the
+                // caller has waited for.  After its last key tile, O_q is published to the softmax.
+                auto issue_pv = [&](int q, int t, int s) -> bool {
+                    uint32_t& pv_n = q == 0 ? pv_n0 : pv_n1;
+                    if (!w.wait(pfull(q), pv_n & 1u, kDevErrMmaFull)) return false;
+                    ++pv_n;
+                    tcgen05_fence_after();
+                    const uint32_t v_s = sb + Cfg::OFF_V + s * Cfg::KV_BYTES;
+                    const uint32_t p_t = tmem_base + Cfg::T_S + q * 128 + Cfg::P_COL;
 #pragma unroll
-                for (int k = 0; k < Cfg::BKV / 16; ++k) {
-                    // P: 16 keys = 8 TMEM columns per step; V: MN-major, 64-column chunks 16 KB
-                    // apart, 16 key rows = 2048 bytes per step
-                    const uint64_t bd = smem_desc_sw128(v_s + k * 2048, Cfg::CHUNK_BYTES, 1024);
-                    mma_f16_ts(tmem_base + Cfg::T_O + q * D, p_t + k * 8, bd, Cfg::IDESC_PV,
-                               (t > 0 || k > 0) ? 1u : 0u);
-                }
-                if (t == (q == 0 ? nkv[0] : nkv[NQ - 1]) - 1) mma_commit(odone(q));
-                return true;
-            };
-            bool ok = w.wait(qfull, 0, kDevErrMmaFull);
-            for (int j = 0; ok && j < nkv_max; ++j) {
-                const int s = j & 1;
-                if (!w.wait(full(s), (j >> 1) & 1u, kDevErrMmaFull)) {   // K_j and V_{j-1}
-                    ok = false;
-                    break;
-                }
-                tcgen05_fence_after();
-                const uint32_t k_s = sb + Cfg::OFF_K + s * Cfg::KV_BYTES;
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    if (j > 0 && j <= nkv[q] && !(ok = issue_pv(q, j - 1))) break;
-                    if (j < nkv[q]) {
-                        // S_q(j) = Q_q K_j^T, over P_q(j-1) (read by the PV just issued)
-                        const uint32_t q_s = sb + Cfg::OFF_Q + q * Cfg::Q_BYTES;
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t off = (k >> 2) * Cfg::CHUNK_BYTES + (k & 3) * 32;
-                            mma_f16_ss(tmem_base + Cfg::T_S + q * 128, smem_desc_sw128(q_s + off, 16, 1024),
-                                       smem_desc_sw128(k_s + off, 16, 1024), Cfg::IDESC_S, k > 0 ? 1u : 0u);
-                        }
-                        mma_commit(sfull(q));
+                    for (int k = 0; k < Cfg::BKV / 16; ++k) {
+                        // P: 16 keys = 8 TMEM columns per step; V: MN-major, 64-column chunks 16 KB
+                        // apart, 16 key rows = 2048 bytes per step
+                        const uint64_t bd = smem_desc_sw128(v_s + k * 2048, Cfg::CHUNK_BYTES, 1024);
+                        mma_f16_ts(tmem_base + Cfg::T_O + q * D, p_t + k * 8, bd, Cfg::IDESC_PV,
+                                   (t > 0 || k > 0) ? 1u : 0u);
                     }
+                    if (t == (q == 0 ? it.nkv[0] : it.nkv[NQ - 1]) - 1) mma_commit(odone(q));
+                    return true;
+                };
+                for (int j = 0; ok && j < it.nkv_max; ++j, ++g) {
+                    const int s = (int)(g & 1u);
+                    if (!w.wait(full(s), (g >> 1) & 1u, kDevErrMmaFull)) {   // K_j and V_{j-1}
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after();
+                    const uint32_t k_s = sb + Cfg::OFF_K + s * Cfg::KV_BYTES;
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        if (j > 0 && j <= it.nkv[q] && !(ok = issue_pv(q, j - 1, s))) break;
+                        if (j < it.nkv[q]) {
+                            // S_q(j) = Q_q K_j^T, over P_q(j-1) (read by the PV just issued, or by
+                            // the previous item's last PV_q: one thread's products complete in order)
+                            const uint32_t q_s = sb + Cfg::OFF_Q + q * Cfg::Q_BYTES;
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t off = (k >> 2) * Cfg::CHUNK_BYTES + (k & 3) * 32;
+                                mma_f16_ss(tmem_base + Cfg::T_S + q * 128, smem_desc_sw128(q_s + off, 16, 1024),
+                                           smem_desc_sw128(k_s + off, 16, 1024), Cfg::IDESC_S, k > 0 ? 1u : 0u);
+                            }
+                            mma_commit(sfull(q));
+                        }
+                    }
+                    if (!ok) break;
+                    // every Q K^T product of the item is issued: Q may be replaced once they finish
+                    if (j == it.nkv_max - 1) mma_commit(qfree);
+                    mma_commit(empty(s));
                 }
                 if (!ok) break;
-                mma_commit(empty(s));
-            }
-            // last entry: V_{nkv_max-1} for the final products of the tiles that need it
-            if (ok) ok = w.wait(full(nkv_max & 1), (nkv_max >> 1) & 1u, kDevErrMmaFull);
-            tcgen05_fence_after();
+                // last entry: V_{nkv_max-1} for the final products of the tiles that need it
+                {
+                    const int s = (int)(g & 1u);
+                    if (!w.wait(full(s), (g >> 1) & 1u, kDevErrMmaFull)) break;
+                    tcgen05_fence_after();
 #pragma unroll
-            for (int q = 0; q < NQ; ++q)
-                if (ok && nkv[q] == nkv_max) ok = issue_pv(q, nkv_max - 1);
-            if (ok) mma_commit(empty(nkv_max & 1));
+                    for (int q = 0; q < NQ; ++q)
+                        if (ok && it.nkv[q] == it.nkv_max) ok = issue_pv(q, it.nkv_max - 1, s);
+                    if (!ok) break;
+                    mma_commit(empty(s));
+                    ++g;
+                }
+            }
             mma_commit(drain);
             w.drain(drain, 0);
         }
@@ -256,149 +330,162 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int q = (warp - 2) >> 2;               // query tile of this group
         const int quad = warp & 3;
         const int r = quad * 32 + lane;              // query row in the tile == TMEM lane
-        const int qi = q_base + q * Cfg::BQ + r;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
         const uint32_t s_col = lane_base + Cfg::T_S + q * 128;
         const uint32_t o_col = lane_base + Cfg::T_O + q * D;
         const bool scale_pos = p.scale_log2 >= 0.0f;
         const float sl2 = p.scale_log2;
-        const int k_lim = p.causal ? min(p.Skv, qi + p.causal_offset + 1) : p.Skv;   // keys < k_lim
-        const int nkv_q = q == 0 ? nkv[0] : nkv[NQ - 1];
-        float m = -INFINITY, l = 0.0f;
+        uint32_t n_item = 0, s_n = 0, o_n = 0;       // items taken; sfull / odone phases waited for
         bool ok = true;
+        while (ok) {
+            const uint32_t box = n_item & 1u;
+            if (!__all_sync(0xffffffffu, w.wait(item_pub(box), (n_item >> 1) & 1u, kDevErrEpilogueFull))) break;
+            const int item = item_box[box];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(item_read(box));
+            ++n_item;
+            if (item < 0) break;
+            const Item it = decode(item);
+            const int qi = it.q_base + q * Cfg::BQ + r;
+            const int k_lim = p.causal ? min(p.Skv, qi + p.causal_offset + 1) : p.Skv;   // keys < k_lim
+            const int nkv_q = q == 0 ? it.nkv[0] : it.nkv[NQ - 1];
+            float m = -INFINITY, l = 0.0f;
 
-        for (int j = 0; j < nkv_q; ++j) {
-            // the warp agrees before any .sync.aligned TMEM access
-            if (!__all_sync(0xffffffffu, w.wait(sfull(q), j & 1, kDevErrEpilogueFull))) {
-                ok = false;
-                break;
-            }
-            tcgen05_fence_after();
-            const int k0 = j * Cfg::BKV;
-            const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
-            // The row's 128 scores are four 32-column chunks c0..c3, all four loaded before
-            // one wait.  `masked` differs between rows of one warp on a diagonal tile, so every TMEM
-            // access stays outside the branches.
-            float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
-            float mt = -INFINITY;                        // masked tiles: running max, scaled
-            auto chunk_max = [&](const uint32_t (&rr)[32], int c) {
-                if (!masked) {
-                    if (scale_pos) {
+            for (int j = 0; j < nkv_q; ++j) {
+                // the warp agrees before any .sync.aligned TMEM access
+                if (!__all_sync(0xffffffffu, w.wait(sfull(q), s_n & 1u, kDevErrEpilogueFull))) {
+                    ok = false;
+                    break;
+                }
+                ++s_n;
+                tcgen05_fence_after();
+                const int k0 = j * Cfg::BKV;
+                const bool masked = k0 + Cfg::BKV > k_lim;   // only the diagonal / last tile of a row
+                // The row's 128 scores are four 32-column chunks c0..c3, all four loaded before
+                // one wait.  `masked` differs between rows of one warp on a diagonal tile, so every TMEM
+                // access stays outside the branches.
+                float e0 = scale_pos ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
+                float mt = -INFINITY;                        // masked tiles: running max, scaled
+                auto chunk_max = [&](const uint32_t (&rr)[32], int c) {
+                    if (!masked) {
+                        if (scale_pos) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            e0 = max3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
-                            e1 = max3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-                            e2 = max3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
-                            e3 = max3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
+                            for (int i = 0; i < 32; i += 8) {
+                                e0 = max3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
+                                e1 = max3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+                                e2 = max3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
+                                e3 = max3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 8) {
+                                e0 = min3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
+                                e1 = min3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+                                e2 = min3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
+                                e3 = min3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
+                            }
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            e0 = min3f(e0, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]));
-                            e1 = min3f(e1, __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-                            e2 = min3f(e2, __uint_as_float(rr[i + 4]), __uint_as_float(rr[i + 5]));
-                            e3 = min3f(e3, __uint_as_float(rr[i + 6]), __uint_as_float(rr[i + 7]));
+                        for (int i = 0; i < 32; ++i)
+                            if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * sl2);
+                    }
+                };
+                // pass 1: maximum of the scaled, masked scores of the row, in log2 units.  The whole
+                // row (128 scores) comes into registers with one wait and stays there for pass 2.
+                uint32_t sc0[32], sc1[32], sc2[32], sc3[32];
+                tmem_ld_32x32b_x32(s_col + 0, sc0);
+                tmem_ld_32x32b_x32(s_col + 32, sc1);
+                tmem_ld_32x32b_x32(s_col + 64, sc2);
+                tmem_ld_32x32b_x32(s_col + 96, sc3);
+                tmem_ld_wait(sc0);
+                reg_tie(sc1);
+                reg_tie(sc2);
+                reg_tie(sc3);
+                chunk_max(sc0, 0);
+                chunk_max(sc1, 1);
+                chunk_max(sc2, 2);
+                chunk_max(sc3, 3);
+                if (!masked)
+                    mt = (scale_pos ? max3f(fmaxf(e0, e1), e2, e3) : min3f(fminf(e0, e1), e2, e3)) * sl2;
+                // lazy move of the exponent base: only by more than 2^RESCALE_LOG2 (always from -inf)
+                float factor = 1.0f;
+                const bool bump = mt > m + Cfg::RESCALE_LOG2;
+                if (bump) {
+                    factor = (m == -INFINITY) ? 0.0f : ex2_approx(m - mt);
+                    m = mt;
+                }
+                l *= factor;
+                const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+                // pass 2: P = 2^(x - m) in fp16, two keys per column, chunk c to columns
+                // 64 + 16c .. +15 of the S region (free: every score is in registers)
+                float ls0 = 0.0f, ls1 = 0.0f;
+                auto chunk_p = [&](const uint32_t (&rr)[32], int c) {
+                    uint32_t packed[16];
+                    if (!masked) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float x0, x1;
+                            ffma2(x0, x1, __uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]), sl2, sl2,
+                                  neg_m, neg_m);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            fadd2(ls0, ls1, p0, p1);
+                            __half2 h = __floats2half2_rn(p0, p1);
+                            packed[i] = *reinterpret_cast<uint32_t*>(&h);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int kk = k0 + c * 32 + 2 * i;
+                            float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), sl2, neg_m));
+                            float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), sl2, neg_m));
+                            if (kk >= k_lim || m == -INFINITY) p0 = 0.0f;
+                            if (kk + 1 >= k_lim || m == -INFINITY) p1 = 0.0f;
+                            ls0 += p0;
+                            ls1 += p1;
+                            __half2 h = __floats2half2_rn(p0, p1);
+                            packed[i] = *reinterpret_cast<uint32_t*>(&h);
                         }
                     }
-                } else {
+                    tmem_st_32x32b_x16(s_col + Cfg::P_COL + c * 16, packed);
+                };
+                chunk_p(sc0, 0);
+                chunk_p(sc1, 1);
+                chunk_p(sc2, 2);
+                chunk_p(sc3, 3);
+                if (j > 0 && __any_sync(0xffffffffu, bump)) {
+                    // O_q (this warp's rows) *= factor: PV_q(j-1) completed before S_q(j) did, and
+                    // PV_q(j) waits for the arrival below; done after pass 2, when the scores are dead
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (k0 + c * 32 + i < k_lim) mt = fmaxf(mt, __uint_as_float(rr[i]) * sl2);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t rr[32];
+                        tmem_ld_32x32b_x32(o_col + c * 32, rr);
+                        tmem_ld_wait(rr);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float y0, y1;
+                            fmul2(y0, y1, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]), factor, factor);
+                            rr[i] = __float_as_uint(y0);
+                            rr[i + 1] = __float_as_uint(y1);
+                        }
+                        tmem_st_32x32b_x32(o_col + c * 32, rr);
+                    }
                 }
-            };
-            // pass 1: maximum of the scaled, masked scores of the row, in log2 units.  The whole
-            // row (128 scores) comes into registers with one wait and stays there for pass 2.
-            uint32_t sc0[32], sc1[32], sc2[32], sc3[32];
-            tmem_ld_32x32b_x32(s_col + 0, sc0);
-            tmem_ld_32x32b_x32(s_col + 32, sc1);
-            tmem_ld_32x32b_x32(s_col + 64, sc2);
-            tmem_ld_32x32b_x32(s_col + 96, sc3);
-            tmem_ld_wait(sc0);
-            reg_tie(sc1);
-            reg_tie(sc2);
-            reg_tie(sc3);
-            chunk_max(sc0, 0);
-            chunk_max(sc1, 1);
-            chunk_max(sc2, 2);
-            chunk_max(sc3, 3);
-            if (!masked)
-                mt = (scale_pos ? max3f(fmaxf(e0, e1), e2, e3) : min3f(fminf(e0, e1), e2, e3)) * sl2;
-            // lazy move of the exponent base: only by more than 2^RESCALE_LOG2 (always from -inf)
-            float factor = 1.0f;
-            const bool bump = mt > m + Cfg::RESCALE_LOG2;
-            if (bump) {
-                factor = (m == -INFINITY) ? 0.0f : ex2_approx(m - mt);
-                m = mt;
+                tmem_st_wait();
+                tcgen05_fence_before();
+                mbar_arrive(pfull(q));           // P_q(j) (and a rescaled O_q) ready for the MMA
+                l += ls0 + ls1;
             }
-            l *= factor;
-            const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-            // pass 2: P = 2^(x - m) in fp16, two keys per column, chunk c to columns
-            // 64 + 16c .. +15 of the S region (free: every score is in registers)
-            float ls0 = 0.0f, ls1 = 0.0f;
-            auto chunk_p = [&](const uint32_t (&rr)[32], int c) {
-                uint32_t packed[16];
-                if (!masked) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0, x1;
-                        ffma2(x0, x1, __uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]), sl2, sl2,
-                              neg_m, neg_m);
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        fadd2(ls0, ls1, p0, p1);
-                        __half2 h = __floats2half2_rn(p0, p1);
-                        packed[i] = *reinterpret_cast<uint32_t*>(&h);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int kk = k0 + c * 32 + 2 * i;
-                        float p0 = ex2_approx(fmaf(__uint_as_float(rr[2 * i]), sl2, neg_m));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(rr[2 * i + 1]), sl2, neg_m));
-                        if (kk >= k_lim || m == -INFINITY) p0 = 0.0f;
-                        if (kk + 1 >= k_lim || m == -INFINITY) p1 = 0.0f;
-                        ls0 += p0;
-                        ls1 += p1;
-                        __half2 h = __floats2half2_rn(p0, p1);
-                        packed[i] = *reinterpret_cast<uint32_t*>(&h);
-                    }
-                }
-                tmem_st_32x32b_x16(s_col + Cfg::P_COL + c * 16, packed);
-            };
-            chunk_p(sc0, 0);
-            chunk_p(sc1, 1);
-            chunk_p(sc2, 2);
-            chunk_p(sc3, 3);
-            if (j > 0 && __any_sync(0xffffffffu, bump)) {
-                // O_q (this warp's rows) *= factor: PV_q(j-1) completed before S_q(j) did, and
-                // PV_q(j) waits for the arrival below; done after pass 2, when the scores are dead
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld_32x32b_x32(o_col + c * 32, rr);
-                    tmem_ld_wait(rr);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float y0, y1;
-                        fmul2(y0, y1, __uint_as_float(rr[i]), __uint_as_float(rr[i + 1]), factor, factor);
-                        rr[i] = __float_as_uint(y0);
-                        rr[i + 1] = __float_as_uint(y1);
-                    }
-                    tmem_st_32x32b_x32(o_col + c * 32, rr);
-                }
+            // output: O_q / l in fp16, and the log-sum-exp.  The next item's first PV_q, which
+            // overwrites O_q, waits for this group's next P, issued only after these loads.
+            if (ok && nkv_q > 0) {
+                ok = __all_sync(0xffffffffu, w.wait(odone(q), o_n & 1u, kDevErrEpilogueFull));
+                ++o_n;
+                tcgen05_fence_after();
             }
-            tmem_st_wait();
-            tcgen05_fence_before();
-            mbar_arrive(pfull(q));           // P_q(j) (and a rescaled O_q) ready for the MMA
-            l += ls0 + ls1;
-        }
-        // epilogue: O_q / l in fp16, and the log-sum-exp
-        if (ok && nkv_q > 0) {
-            ok = __all_sync(0xffffffffu, w.wait(odone(q), 0, kDevErrEpilogueFull));
-            tcgen05_fence_after();
-        }
-        if (ok) {
+            if (!ok) break;
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            uint4* dst = reinterpret_cast<uint4*>(p.O + ((size_t)bh * p.Sq + qi) * D);
+            uint4* dst = reinterpret_cast<uint4*>(p.O + ((size_t)it.bh * p.Sq + qi) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t rr[32];
@@ -424,7 +511,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
             }
             if (p.lse && qi < p.Sq)
-                p.lse[(size_t)bh * p.Sq + qi] = l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                p.lse[(size_t)it.bh * p.Sq + qi] = l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            tcgen05_fence_before();
         }
     }
 
@@ -446,7 +534,7 @@ __global__ void gsr_attention_empty_kernel(__half* O, float* lse, long long rows
 
 template <class Cfg>
 cudaError_t launch_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const AttnParams& p, cudaStream_t stream) {
+                       const AttnParams& p, int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -458,19 +546,17 @@ cudaError_t launch_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const int rows_per_cta = Cfg::NQ * Cfg::BQ;
-    const long long blocks = (long long)((p.Sq + rows_per_cta - 1) / rows_per_cta) * p.BH;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    gsr_attention_kernel<Cfg><<<(unsigned)blocks, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    if (grid <= 0 || grid > p.num_items) return cudaErrorInvalidValue;
+    gsr_attention_kernel<Cfg><<<(unsigned)grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             const AttnParams& p, int D, cudaStream_t stream) {
-    if (D == 64) return launch_cfg<AttnCfg<64>>(tmQ, tmK, tmV, p, stream);
-    if (D == 128) return launch_cfg<AttnCfg<128>>(tmQ, tmK, tmV, p, stream);
+                             const AttnParams& p, int D, int grid, cudaStream_t stream) {
+    if (D == 64) return launch_cfg<AttnCfg<64>>(tmQ, tmK, tmV, p, grid, stream);
+    if (D == 128) return launch_cfg<AttnCfg<128>>(tmQ, tmK, tmV, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -29,8 +29,12 @@ std::atomic<int> g_raster_group{0};   // 0: each kernel's default grouping
 constexpr int kSkinnyMaxM = 64;
 constexpr int kGroupM = 16;
 
+// Device words per (device, stream): [0] the error word of kernels on the stream, [1] and [2]
+// the attention kernel's work counter and done count (zero between launches).
+constexpr int kStreamWords = 4;
+
 struct StreamState {
-    int* err = nullptr;          // device error word for kernels on this stream
+    int* err = nullptr;          // kStreamWords device words, the error word first
     float* partials = nullptr;   // small-M split-K partial tiles
     size_t partial_floats = 0;
     int* tickets = nullptr;      // small-M per-tile ticket counters (zero between launches)
@@ -202,11 +206,12 @@ gsr_status stream_state(int dev, cudaStream_t stream, size_t need_partials, size
     StreamState& s = g_streams[{dev, stream}];
     cudaError_t e;
     if (!s.err) {
-        if ((e = cudaMalloc(&s.err, sizeof(int))) != cudaSuccess) {
+        if ((e = cudaMalloc(&s.err, kStreamWords * sizeof(int))) != cudaSuccess) {
             s.err = nullptr;
             return cuda_fail(e);
         }
-        if ((e = cudaMemsetAsync(s.err, 0, sizeof(int), stream)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemsetAsync(s.err, 0, kStreamWords * sizeof(int), stream)) != cudaSuccess)
+            return cuda_fail(e);
     }
     if (need_partials > s.partial_floats || need_tickets > s.ticket_count) {
         // Earlier launches on this stream may still use the old buffers.
@@ -721,12 +726,17 @@ gsr_status flash_attention_fwd(const void* Q, const void* K, const void* V, void
         if (g > (uint64_t)BH) g = (uint64_t)BH;
         p.head_group = (int)g;
     }
+    const int64_t items = (seq_q + 255) / 256 * BH;
+    if (items > INT_MAX) return GSR_ERR_INVALID_ARG;
+    p.num_items = (int)items;
+    p.work = ss.err + 1;
     p.O = static_cast<__half*>(O);
     p.lse = lse;
     p.err = ss.err;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.test_flags = g_test_flags.load(std::memory_order_relaxed);
-    e = gsr::launch_attention(tmQ, tmK, tmV, p, (int)head_dim, st);
+    const int grid = items < info.num_sms ? (int)items : info.num_sms;   // one CTA per SM
+    e = gsr::launch_attention(tmQ, tmK, tmV, p, (int)head_dim, grid, st);
     return e == cudaSuccess ? GSR_OK : cuda_fail(e);
 }
 

@@ -96,7 +96,9 @@ struct AttnParams {
     int causal;             // keep key k for query q when k <= q + causal_offset
     int causal_offset;      // Skv - Sq
     float scale_log2;       // softmax scale * log2(e)
-    int head_group;         // launch order: query blocks longest first within groups of this many heads
+    int head_group;         // item order: query blocks longest first within groups of this many heads
+    int num_items;          // ceil(Sq / 256) * BH work items (two 128-query tiles of one head each)
+    int* work;              // [0] the launch's next work item, [1] CTAs done taking items; 0 between launches
     __half* O;              // (BH, Sq, D) row-major
     float* lse;             // optional (BH, Sq): natural-log log-sum-exp of the scaled scores
     int* err;
@@ -104,9 +106,10 @@ struct AttnParams {
     uint32_t test_flags;
 };
 
-// Attention forward: Q, K, V as 3-D tensor maps {D, seq, BH} with 64 x 128 x 1 boxes.
+// Attention forward: Q, K, V as 3-D tensor maps {D, seq, BH} with 64 x 128 x 1 boxes; a
+// persistent grid of `grid` CTAs (one per SM at most) takes the p.num_items work items.
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             const AttnParams& p, int D, cudaStream_t stream);
+                             const AttnParams& p, int D, int grid, cudaStream_t stream);
 // O = 0, lse = -inf for `rows` rows of width D (no keys).
 cudaError_t launch_attention_empty(__half* O, float* lse, long long rows, int D, cudaStream_t stream);
 
