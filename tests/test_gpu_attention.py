@@ -132,3 +132,38 @@ def test_validation():
                          128, d, ctypes.c_float(0.0), 0, None)
     assert L.flash_attention_fwd(*args(t.data_ptr(), 96)) == gsr.Status.ERR_INVALID_ARG
     assert L.flash_attention_fwd(*args(t.data_ptr(), 64)) == gsr.Status.ERR_ALIAS
+
+
+# Many work items per CTA: the kernel runs one persistent CTA per SM (152 on GB300), each taking
+# (two query tiles, batch x head) items from a device counter one after another, with one item's
+# last products overlapping the next item's first.  These shapes have 2-3 items per CTA.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,S,D", [(4, 40, 512, 64), (2, 80, 700, 128), (3, 33, 1280, 128)])
+def test_many_items_per_cta(B, H, S, D, causal):
+    check(*inputs(B, H, S, S, D, seed=B * H + S + D), causal=causal)
+
+
+@pytest.mark.parametrize("Sq,Skv,D", [(1024, 300, 128), (900, 1300, 64)])
+def test_many_items_with_keyless_items_between(Sq, Skv, D):
+    # causal with Sq > Skv: the first query blocks of every head have no key at all (O = 0,
+    # lse = -inf), so items without work sit between items with work in every CTA's sequence
+    check(*inputs(2, 100, Sq, Skv, D, seed=Sq + Skv), causal=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bench_workload_sampled_heads(causal):
+    # The benchmarked attention workload in full (4 x 32 heads, 4096 x 4096, D 128; 2048 items on
+    # 152 CTAs), checked on a sample of heads against the oracle.
+    from tensor_core_gemm_multistage_gb300.workloads import ATTN_WORKLOADS, attention_inputs
+    w = ATTN_WORKLOADS["attn_b4_h32_s4096_d128"]
+    q, k, v = attention_inputs(w, seed=0)
+    o, lse = run(q, k, v, causal=causal)
+    for b, h in ((0, 0), (1, 17), (3, 31)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref, ref_lse, _ = attention(q[sl], k[sl], v[sl], causal=causal, return_lse=True)
+        x = o[sl].astype(np.float64)
+        y = ref.astype(np.float64)
+        assert not np.isnan(x).any()
+        assert np.all(np.abs(x - y) <= 1e-2 + 1e-2 * np.abs(y)), (b, h)
+        assert np.linalg.norm(x - y) / np.linalg.norm(y) <= 2e-3, (b, h)
+        assert np.all(np.abs(lse[sl] - ref_lse) <= 1e-3), (b, h)
