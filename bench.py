@@ -464,7 +464,7 @@ def run_gsr(args, w):
     kernel = KERNEL_NAMES[path]
     peaks, peaks_src = measured_peaks()
 
-    sampler = ClockSampler(gpu_uuid(), interval_ms=50).start() if rank == 0 else None
+    sampler = ClockSampler(gpu_uuid(), interval_ms=20).start() if rank == 0 else None
     rec, (A, B, dA, dB, dC, flush, step) = time_gemm(gsr, w, args, dev, stream, world, args.epilogue)
     t_wall0, t_wall1 = rec["wall"]
     inputs_bytes = (w.M * w.K + w.K * w.N) * 2

@@ -167,3 +167,25 @@ def test_bench_workload_sampled_heads(causal):
         assert np.all(np.abs(x - y) <= 1e-2 + 1e-2 * np.abs(y)), (b, h)
         assert np.linalg.norm(x - y) / np.linalg.norm(y) <= 2e-3, (b, h)
         assert np.all(np.abs(lse[sl] - ref_lse) <= 1e-3), (b, h)
+
+
+def test_two_streams_at_once_keep_their_own_work_counters():
+    # Each stream has its own item counter: two persistent launches running at the same time on
+    # two streams must each process exactly their own items, call after call.
+    dev = torch.device("cuda", 0)
+    cases = [inputs(2, 60, 640, 640, 128, seed=41), inputs(3, 50, 512, 700, 64, seed=42)]
+    dq = [tuple(t.to(dev) for t in c) for c in cases]
+    outs = [torch.full(c[0].shape, float("nan"), dtype=torch.float16, device=dev) for c in cases]
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (q, k, v), o, s, causal in zip(dq, outs, streams, (True, False)):
+            with torch.cuda.stream(s):
+                gsr.flash_attention_fwd(q, k, v, o, causal=causal, stream=s)
+    for s in streams:
+        assert gsr.device_status(s)[0] == gsr.Status.OK
+    for (q, k, v), o, causal in zip(cases, outs, (True, False)):
+        ref = attention(q, k, v, causal=causal).astype(np.float64)
+        x = o.cpu().numpy().astype(np.float64)
+        assert not np.isnan(x).any()
+        assert np.all(np.abs(x - ref) <= 1e-2 + 1e-2 * np.abs(ref))
