@@ -49,7 +49,7 @@ KERNEL_SOURCES = {
     "gsr_tiled_kernel": ["csrc/gemm_tiled.cu"] + _SHARED_SOURCES,
     "gsr_pair_kernel": ["csrc/gemm_pair.cu"] + _SHARED_SOURCES,
     "gsr_skinny_kernel": ["csrc/gemm_skinny.cu"] + _SHARED_SOURCES,
-    "gsr_attention_kernel": ["csrc/attention_fwd.cu"] + _SHARED_SOURCES,
+    "gsr_attention_kernel": ["csrc/attention_fwd.cu", "csrc/attention.h"] + _SHARED_SOURCES,
 }
 KERNEL_NAMES = {0: "gsr_tiled_kernel", 1: "gsr_skinny_kernel", 2: "gsr_pair_kernel", 3: "gsr_pair_kernel"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")

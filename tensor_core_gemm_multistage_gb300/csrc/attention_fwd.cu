@@ -27,6 +27,7 @@
 #include <atomic>
 
 #include "device_common.cuh"
+#include "attention.h"
 #include "kernels.h"
 
 namespace gsr {

@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "gsr.h"
+#include "attention.h"
 #include "kernels.h"
 
 namespace {
