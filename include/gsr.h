@@ -192,9 +192,10 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
  * Calls whose work overlaps on the GPU (for example on two streams with no
  * ordering between them) race on the array and produce wrong results: order
  * them on one stream.  If a bounded wait inside the kernel runs out, C is left
- * unspecified; gsr_device_status (on any stream of that device) reports
- * GSR_ERR_DEVICE_TIMEOUT for the most recent call of this entry point there,
- * until it has been read once or the next call starts.
+ * unspecified; gsr_device_status reports GSR_ERR_DEVICE_TIMEOUT for the most
+ * recent call of this entry point on the current device, until it has been read
+ * once or the next call starts.  It reads the word after the work of the stream it
+ * is given: pass the stream the call was queued on (or one ordered after it).
  */
 gsr_status gemm_scale_relu_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
                                    int64_t K, float alpha, struct CUstream_st* stream);
