@@ -71,10 +71,11 @@ typedef enum gsr_status {
  * there are enough of them to fill the GPU, else one CTA per 128-row tile.
  *
  * Device memory the library owns: on the first call on each (device, stream)
- * pair it allocates a 4-byte error word for that stream, and the small-M
- * kernel keeps fp32 partial tiles and per-tile ticket counters in a workspace
- * allocated (or grown) on the first small-M call on the pair.  Both stay
- * until gsr_release_stream() for that stream or gsr_shutdown().  Calls on different streams never share them; such a
+ * pair it allocates 16 bytes for that stream (the kernels' error word and the
+ * attention kernel's work counters), and the small-M kernel keeps fp32 partial
+ * tiles and per-tile ticket counters in a workspace allocated (or grown) on the
+ * first small-M call on the pair.  Both stay until gsr_release_stream() for that
+ * stream or gsr_shutdown().  Calls on different streams never share them; such a
  * first call synchronises its stream and so should not be made during stream
  * capture.  Once a stream has seen a call of the same kind (and size, for the
  * small-M workspace), further calls on it only encode tensor maps on the host
@@ -220,7 +221,7 @@ gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
 
 /*
  * Releases the library's state for the (current device, stream) pair: the
- * stream's 4-byte error word and, if a small-M call ran on it, its workspace.
+ * stream's 16 bytes of words and, if a small-M call ran on it, its workspace.
  * Waits for the stream first (queued kernels may still use them).  For callers
  * that create and destroy streams: call it before destroying a stream the
  * library was used on, from no other thread launching on that stream at the same
