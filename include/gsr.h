@@ -80,7 +80,10 @@ typedef enum gsr_status {
  * capture.  Once a stream has seen a call of the same kind (and size, for the
  * small-M workspace), further calls on it only encode tensor maps on the host
  * and launch, so they can be captured into a CUDA graph and replayed; a
- * replay reads whatever the captured buffers hold then.
+ * replay reads whatever the captured buffers hold then.  A captured call keeps
+ * using the capture stream's library memory (error word, attention work
+ * counters, small-M workspace): replays must not run at the same time as each
+ * other or as other library calls on that stream.
  */
 gsr_status gemm_scale_relu(const void* A, const void* B, void* C, int64_t M, int64_t N,
                            int64_t K, float alpha, struct CUstream_st* stream);
