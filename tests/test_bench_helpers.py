@@ -43,3 +43,37 @@ def test_source_hash_ignores_comments_but_not_code():
     code = "int f(int x) {\n    return x + 1;  // add one\n}\n/* block\n comment */\n"
     assert bench._code_only(code) == bench._code_only("int f(int x) { return x + 1; }")
     assert bench._code_only(code) != bench._code_only("int f(int x) { return x + 2; }")
+
+
+def test_gemm_roofline_bounds_and_fractions():
+    from tensor_core_gemm_multistage_gb300.workloads import WORKLOADS
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    w = WORKLOADS["llm_mlp_up"]
+    r = bench.gemm_roofline(w, 2, "gsr_pair_kernel", 1.0, 20.0, peaks, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - w.flops / 1e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / 1900.0) < 1e-12            # a 20 ms region: burst peak
+    r = bench.gemm_roofline(w, 2, "gsr_pair_kernel", 1.0, 800.0, peaks, "measured")
+    assert r["peak"] == 1700.0                                        # >= 0.5 s: sustained peak
+    s = WORKLOADS["skinny_decode"]
+    r = bench.gemm_roofline(s, 1, "gsr_skinny_kernel", 0.08, 16.0, peaks, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - s.bytes / 0.08e-3 / 1e9) < 1e-6 and abs(r["frac"] - r["achieved"] / 6800.0) < 1e-12
+
+
+def test_per_config_entry_fields():
+    from tensor_core_gemm_multistage_gb300.workloads import WORKLOADS
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    w = WORKLOADS["skinny_decode"]
+    rec = {"step_ms": 0.1, "kernel_ms": 0.08, "median5_ms": 0.09, "region_ms": 2.0, "l2": "x"}
+    e = bench.per_config_entry(w, rec, 1, "gsr_skinny_kernel", peaks, "measured", 1)
+    assert e["kernel"] == "gsr_skinny_kernel" and e["ms_per_step"] == 0.1
+    assert abs(e["TFLOP/s"] - w.flops / 0.1e-3 / 1e12) < 1e-9
+    assert abs(e["median5_TFLOP/s"] - w.flops / 0.09e-3 / 1e12) < 1e-9
+    assert abs(e["GB/s"] - w.bytes / 0.08e-3 / 1e9) < 1e-6
+    assert e["roofline"]["bound"] == "hbm"
+
+
+def test_host_cpu_model_is_a_string():
+    m = bench.host_cpu_model()
+    assert isinstance(m, str) and m
