@@ -432,6 +432,31 @@ def time_gemm(gsr, w, args, dev, stream, world, epilogue="scale_relu"):
     return rec, (A, B, dA, dB, dC, flush, step)
 
 
+def oracle_baseline(A, B, w, seconds: float):
+    """The CPU oracle on one configuration: all of C when that fits in about `seconds` (the
+    per-row time measured on one chunk of rows first), else whole rows until `seconds` have
+    passed, with the full time extrapolated from the per-row time (and labelled so)."""
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    chunk = min(w.M, threads)
+    t = time.perf_counter()
+    oracle.gemm_scale_relu(A, B, w.alpha, rows=list(range(chunk)))
+    per_row = max(time.perf_counter() - t, 1e-9) / chunk
+    if per_row * w.M <= seconds:
+        t = time.perf_counter()
+        oracle.gemm_scale_relu(A, B, w.alpha)
+        secs = time.perf_counter() - t
+        return {"value": w.flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                "sample": "all %d rows of C, %.2f s" % (w.M, secs), "per_row_ms": secs / w.M * 1e3,
+                "full_s": secs}
+    rows, secs, cores = time_oracle(A, B, w.alpha, seconds)
+    return {"value": 2.0 * rows * w.N * w.K / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "sample": "%d whole rows of C (of %d), %.1f s" % (rows, w.M, secs),
+            "per_row_ms": secs / rows * 1e3, "extrapolated_full_s": secs / rows * w.M,
+            "extrapolated_note": "extrapolated: measured per-row time x M rows, not a full run"}
+
+
 def per_config_entry(w, rec, path, kernel, peaks, peaks_src, world):
     value = whole_job_tflops(world, w.flops, rec["step_ms"])
     e = {"M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha, "kernel": kernel,
@@ -527,10 +552,15 @@ def run_gsr(args, w):
                 continue
             opath = gsr.select_path(ow.M, ow.N, ow.K)
             orec, bufs = time_gemm(gsr, ow, args, dev, stream, world)
+            oA, oB = bufs[0], bufs[1]
             del bufs
             per_config[name] = per_config_entry(ow, orec, opath, KERNEL_NAMES[opath], peaks,
                                                 peaks_src, world)
             torch.cuda.empty_cache()
+            if world == 1 and args.cpu_seconds > 0:
+                # the oracle in full where it takes a few seconds, else a sample of whole rows
+                per_config[name]["cpu_baseline"] = oracle_baseline(oA, oB, ow, min(5.0, args.cpu_seconds))
+            del oA, oB
     if sampler is not None:
         sampler.stop()
 

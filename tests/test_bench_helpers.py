@@ -77,3 +77,14 @@ def test_per_config_entry_fields():
 def test_host_cpu_model_is_a_string():
     m = bench.host_cpu_model()
     assert isinstance(m, str) and m
+
+
+def test_oracle_baseline_full_and_sampled():
+    from tensor_core_gemm_multistage_gb300.workloads import Workload, make_inputs
+    w = Workload("t", 96, 64, 64, 0.5)
+    A, B = make_inputs(w.M, w.N, w.K, seed=1)
+    full = bench.oracle_baseline(A, B, w, 30.0)
+    assert full["kind"] == "oracle" and "full_s" in full and full["sample"].startswith("all 96 rows")
+    sampled = bench.oracle_baseline(A, B, w, 0.0)        # no time for all rows: a labelled sample
+    assert "extrapolated_full_s" in sampled and "extrapolated" in sampled["extrapolated_note"]
+    assert sampled["per_row_ms"] > 0 and sampled["value"] > 0
