@@ -223,7 +223,7 @@ def time_oracle(A, B, alpha, seconds: float):
     threads = oracle.max_threads()
     chunk = min(M, threads)
     done, t_total, row = 0, 0.0, 0
-    while t_total < seconds:
+    while done == 0 or t_total < seconds:          # at least one chunk
         rows = [(row + i) % M for i in range(chunk)]
         t = time.perf_counter()
         oracle.gemm_scale_relu(A, B, alpha, rows=rows)
