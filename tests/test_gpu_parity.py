@@ -379,3 +379,27 @@ def test_pair_kernel_l2_switches(flags):
     finally:
         gsr.set_test_flags(0)
     check(C if rows is None else C[rows], ref, z, "pair flags %d" % flags)
+
+
+# ---------------------------------------------------------------------------- large sizes
+
+def test_a_million_rows():
+    # M = 10^6 (not a multiple of 256): 3907 pair tiles over 76 pairs, tile and raster
+    # arithmetic far from the small cases; checked on a row sample that includes the last rows
+    M, N, K = 1_000_000, 136, 72
+    A, B = make_inputs(M, N, K, seed=77)
+    rows = sorted(set(sample_rows(M)) | {M - 2, M - 129, M - 256, 999_935})
+    C = run_gpu(A, B, 0.5)
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, rows=rows, return_pre=True)
+    check(C[rows], ref, z, "M=10^6")
+
+
+@pytest.mark.parametrize("path", [gsr.PATH_AUTO, gsr.PATH_PAIR, gsr.PATH_TILED_128])
+def test_a_long_k(path):
+    # K = 2^17 - 8: 2048 k-blocks, so every ring slot's phase bit wraps hundreds of times within
+    # one tile, and the last k-block is ragged
+    M, N, K = 200, 256, (1 << 17) - 8
+    A, B = make_inputs(M, N, K, seed=78, b_std_inv_sqrt_k=True)
+    C = run_gpu(A, B, 1.0, path)
+    ref, z = oracle.gemm_scale_relu(A, B, 1.0, return_pre=True)
+    check(C, ref, z, "K=2^17-8 path %d" % path)
