@@ -415,17 +415,19 @@ def time_gemm(gsr, w, args, dev, stream, world, epilogue="scale_relu"):
     kernel_ms = [a.elapsed_time(b) for a, b in ev]
     region_ms = start.elapsed_time(stop)
     step_ms = region_ms / args.steps if flush is None else sum(kernel_ms) / args.steps
-    med = None
+    med, wall_repeats = None, None
     if args.repeats > 0:
         # After the timed region: `repeats` more runs of max(100, steps) back-to-back calls
         # each, timed the same way; the median of their mean call times.
+        tr0 = time.time()
         reps = [run_block(step, max(100, args.steps), stream, flush) for _ in range(args.repeats)]
+        wall_repeats = (tr0, time.time())
         med = statistics.median(reps)
     rec = {
         "step_ms": max_over_ranks(step_ms, world),
         "kernel_ms": max_over_ranks(sum(kernel_ms) / len(kernel_ms), world),
         "median5_ms": max_over_ranks(med, world) if med is not None else None,
-        "region_ms": region_ms, "wall": (t_wall0, t_wall1),
+        "region_ms": region_ms, "wall": (t_wall0, t_wall1), "wall_repeats": wall_repeats,
         "l2": ("inputs larger than L2 (A+B %d MiB > 126 MiB), no flush" % (inputs_bytes >> 20))
         if flush is None else "flush L2 between steps (256 MiB write outside each call's events)",
     }
@@ -591,6 +593,10 @@ def run_gsr(args, w):
         line["per_config"] = per_config
     if sampler is not None:
         line["clocks"] = sampler.summary(t_wall0, t_wall1)
+        if rec["wall_repeats"] is not None:
+            # the timed region is a few tens of ms, so a handful of samples at most; the
+            # median5 repeats run the same kernel for longer and give the clock under load
+            line["clocks"]["median5_window"] = sampler.summary(*rec["wall_repeats"])
     if world == 1 and args.cpu_seconds > 0:
         rows, secs, cores = time_oracle(A, B, w.alpha, args.cpu_seconds)
         per_row_s = secs / rows

@@ -88,3 +88,21 @@ def test_oracle_baseline_full_and_sampled():
     sampled = bench.oracle_baseline(A, B, w, 0.0)        # no time for all rows: a labelled sample
     assert "extrapolated_full_s" in sampled and "extrapolated" in sampled["extrapolated_note"]
     assert sampled["per_row_ms"] > 0 and sampled["value"] > 0
+
+
+def test_clock_summary_windows_and_reasons():
+    s = bench.ClockSampler("GPU-a")
+    idle = ["Not Active"] * 5
+    capped = ["Active", "Not Active", "Not Active", "Not Active", "Active"]
+    s.samples = [(10.00, 2070.0, 2070.0, idle, "GPU-a"),
+                 (10.02, 1980.0, 2070.0, capped, "GPU-a"),
+                 (10.04, 2010.0, 2070.0, idle, "GPU-a"),
+                 (10.02, 900.0, 2070.0, idle, "GPU-b")]       # another GPU's line
+    got = s.summary(10.01, 10.05)
+    assert got["samples"] == 2 and got["window"] == "timed region"
+    assert got["sm_mhz"] == 1995.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"]
+    # a window between two samples falls back to the samples around it
+    near = s.summary(10.041, 10.045)
+    assert near["window"] == "around the timed region" and near["samples"] == 3
+    assert bench.ClockSampler("GPU-x").summary(0, 1)["samples"] == 0
