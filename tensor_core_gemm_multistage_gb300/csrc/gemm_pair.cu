@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 // nothing of this half-tile lies inside C; still release the accumulator
                 tcgen05_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(leader_tempty);
+                if (lane == 0) mbar_arrive_remote(leader_tempty);
             }
             for (int c = 0; c < nchunks; ++c) {
                 uint32_t r0[32], r1[32];
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 if (c == nchunks - 1) {
                     tcgen05_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(leader_tempty);
+                    if (lane == 0) mbar_arrive_remote(leader_tempty);
                 }
                 const uint32_t buf = cidx & 1u;
                 epilogue_store_chunk(r0, r1, smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES,

@@ -460,6 +460,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Arrive on an mbarrier that may live in another CTA of the cluster, with the default (CTA-scope)
+// release: unlike mbar_arrive_cluster it does not first wait for this thread's earlier memory
+// operations to become visible to the whole cluster, which after an issued TMA store costs over
+// a thousand cycles.  For arrivals that publish no memory writes to the other CTA, such as an
+// epilogue warp releasing an accumulator whose tcgen05.ld reads have already completed.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 2-D tiled load into this CTA's shared memory whose completion is counted on an mbarrier
 // that may live in the peer CTA of the pair (the pair's leader).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
