@@ -247,7 +247,7 @@ gsr_status stream_state(int dev, cudaStream_t stream, size_t need_partials, size
 
 // Whole 256 x 256 tiles of a pair launch: all of them, unless the last wave would keep at
 // most half of the pairs busy; then that wave's tiles run as two 256 x 128 halves each, on
-// twice as many pairs (a half costs ~0.56-0.66 of a tile: half the MMAs, at N = 128, and 3/4
+// twice as many pairs (a half costs ~0.6-0.7 of a tile: half the MMAs, at N = 128, and 3/4
 // of the copies).
 int pair_full_tiles(int num_tiles, int clusters, int bn) {
     if (bn != 256 || clusters <= 0) return num_tiles;
@@ -258,29 +258,43 @@ int pair_full_tiles(int num_tiles, int clusters, int bn) {
 // 0: tiled, one CTA per 128 x BN tile; 1: small-M; 2: tiled on CTA pairs (256 x 256 tiles),
 // taken when there are at least as many pair tiles as half the SMs (one full wave of pairs).
 // Pair tiles 256 wide (with a last wave of half tiles where that helps), or 128 wide where
-// that is estimated to be faster: time ~ waves x tile cost, a 256 x 128 tile or half unit
-// costing ~0.56 of a 256 x 256 one in a wave of its own (half the MMAs plus the fixed
-// per-tile part), and the narrower tiles must win by 5 %.
+// that is estimated to be faster: time ~ waves x tile cost, a wave of 256 x 128 tiles or half
+// units costing kHalfTileCost of a wave of 256 x 256 tiles (half the MMAs plus the fixed
+// per-tile part), and the narrower tiles must win by 5 %.  Measured per wave on GB300 (same
+// process, interleaved): 0.61 (4096 x 1280 x 4096), 0.68 (6144^2 x 2048), 0.70 (16384 x 640 x
+// 4096).  At 0.56 the model sent 16384 x 384 and 16384 x 640 (K 4096) to the narrow tiles,
+// 4.7 % and 17 % slower than 256 x 256; now only N <= 128-like shapes, where a 256-wide tile is
+// half empty, take them.
+constexpr double kHalfTileCost = 0.68;
+
 int pair_path(int64_t M, int64_t N, int num_sms) {
     const long long mb = (M + 255) / 256, clusters = num_sms / 2 > 0 ? num_sms / 2 : 1;
     const long long t256 = mb * ((N + 255) / 256);
     const long long full = pair_full_tiles((int)t256, (int)clusters, 256);
-    const double w256 = (double)(full / clusters) + (full < t256 ? 0.56 : (t256 % clusters ? 1.0 : 0.0));
+    const double w256 =
+        (double)(full / clusters) + (full < t256 ? kHalfTileCost : (t256 % clusters ? 1.0 : 0.0));
     const long long w128 = (mb * ((N + 127) / 128) + clusters - 1) / clusters;
-    return 0.56 * (double)w128 < 0.95 * w256 ? 3 : 2;
+    return kHalfTileCost * (double)w128 < 0.95 * w256 ? 3 : 2;
 }
 
-// Tile width of the one-CTA-per-tile kernel: 256 when there are at least half as many
-// 128 x 256 tiles as SMs, else 128.  An N = 256 MMA does twice the work of an N = 128 one in
-// ~1.45x the time and its tile stages less per flop, which outweighs idle SMs down to about
-// half a wave (L2 flushed, mean of 200 calls: 2048^3 with 128 tiles of 128 x 256 19.2 us
-// against 26.9 with 256 of 128 x 128, 1536 x 2048 x 2048 with 96 tiles 19.2 against 25.7),
-// but not below it (64 tiles: 1024 x 2048 x 1024 14.0 against 12.6, 512 x 4096 x 2048 18.7
-// against 17.4; 32 tiles: 1024^3 13.9 against 12.6).  64-wide tiles (path override 7) are a
-// sweep candidate only: on 1024^3 they took the same time as 128-wide ones and lost on every
-// larger shape measured.
+// Tile width of the one-CTA-per-tile kernel: whichever finishes first when a wave of
+// 128 x 256 tiles costs kWideTileCost waves of 128 x 128 tiles (an N = 256 MMA does twice the
+// work of an N = 128 one in ~1.45x the time, and its tile stages 1.5x the bytes per k-block).
+// L2 flushed, mean of 200 calls: 2048^3 with 128 tiles of 128 x 256 19.2 us against 26.9 with
+// 256 of 128 x 128, 1536 x 2048 x 2048 with 96 tiles 19.2 against 25.7, while below half a
+// wave the narrow tiles win (64 tiles: 1024 x 2048 x 1024 14.0 against 12.6, 512 x 4096 x 2048
+// 18.7 against 17.4; 32 tiles: 1024^3 13.9 against 12.6).  Counting waves, not tiles, also
+// keeps N = 128 on 128-wide tiles, where a 256-wide one is half empty (16384 x 128 x 4096:
+// 27.6 against 31.1 us).  64-wide tiles (path override 7) are a sweep candidate only: on 1024^3
+// they took the same time as 128-wide ones and lost on every larger shape measured.
+constexpr double kWideTileCost = 1.45;
+
 int tiled_width(long long mb, int64_t N, int num_sms) {
-    return 2 * mb * ((N + 255) / 256) >= num_sms ? 256 : 128;
+    const long long sms = num_sms > 0 ? num_sms : 1;
+    const long long t256 = mb * ((N + 255) / 256), t128 = mb * ((N + 127) / 128);
+    const double w256 = kWideTileCost * (double)((t256 + sms - 1) / sms);
+    const double w128 = (double)((t128 + sms - 1) / sms);
+    return w256 < w128 ? 256 : 128;
 }
 
 int choose_path(int64_t M, int64_t N, int num_sms) {

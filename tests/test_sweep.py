@@ -27,3 +27,20 @@ def test_sweep_runs_every_candidate():
     assert len(results) == len(sweep.candidates(48, 1024, 512))
     assert all(r["ms"] > 0 and len(r["ms_all"]) == 2 for r in results)
     assert best in results and auto in ("tiled", "small_m", "pair_256x256", "pair_256x128")
+
+
+def test_choice_shapes_straddle_the_pair_threshold():
+    # the boundary list must keep shapes on both sides of 76 pair tiles (half of 152 SMs)
+    tiles = [((M + 255) // 256) * ((N + 255) // 256) for M, N, _ in sweep.CHOICE_SHAPES]
+    assert min(tiles) < 76 <= max(tiles)
+    assert any(70 <= t < 76 for t in tiles) and any(76 <= t <= 81 for t in tiles)
+
+
+@pytest.mark.gpu
+def test_check_choice_runs_on_two_shapes():
+    gsr.build()
+    rows = sweep.check_choice(shapes=[(1024, 1024, 512), (2048, 2560, 512)], rounds=1)
+    assert [r["choice"] for r in rows] == ["tiled", "pair_256x256"]
+    for r in rows:
+        assert set(r["us"]) == set(sweep.CHOICE_KERNELS) and all(t > 0 for t in r["us"].values())
+        assert r["fastest"] in sweep.CHOICE_KERNELS and r["choice_over_fastest"] > 0
