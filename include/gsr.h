@@ -150,10 +150,14 @@ gsr_status flash_attention_fwd(const void* Q, const void* K, const void* V, void
  * complete.  The host buffers should be page-locked (cudaHostAlloc / pinned) for
  * the copies to be asynchronous.  Sizes, alignment and errors as for
  * gemm_scale_relu; dC must not overlap dA or dB.
- * From 2^33 flop (~8.6 GFLOP) and 1024 rows up the three parts overlap: B is copied
- * first, then A in 2..8 chunks of rows; each chunk's product runs on `stream` as
- * soon as its rows have landed and its rows of C go back while later chunks are
- * copied in.  The copies then run on two library-owned streams per device (one
+ * From 2^33 flop (~8.6 GFLOP) and 1024 rows up the three parts overlap: A is copied
+ * in 2..8 chunks of rows, and B whole or, where C has more elements than A and B
+ * together, in 2..4 blocks of columns (each a multiple of 256 columns, wide enough
+ * for a full wave of the CTA-pair kernel); the product of each chunk of rows and
+ * block of columns runs on `stream` as soon as both have landed, and that block of
+ * C goes back (a strided copy) while later ones are copied in.  dB and dC then
+ * hold the whole matrices as for gemm_scale_relu; only the order in which their
+ * parts are written changes.  The copies run on two library-owned streams per device (one
  * per direction, joined to `stream` by library-owned events; created on first
  * use, released by gsr_shutdown), and concurrent calls on one device queue their
  * copies one call after the other.

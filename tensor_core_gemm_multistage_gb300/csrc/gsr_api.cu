@@ -52,10 +52,13 @@ std::map<std::pair<int, CUstream_st*>, StreamState> g_streams;
 
 // Copy streams and events of the pipelined host entry point, one set per device (created on
 // first use, released by gsr_shutdown).  `m` keeps one call's enqueue sequence together.
-constexpr int kHostMaxChunks = 8;
+// Events: start, done, one per row chunk of A, one per column block of B, one per block of C.
+constexpr int kHostMaxChunks = 8;      // row chunks of A and C
+constexpr int kHostMaxColBlocks = 4;   // column blocks of B and C
+constexpr int kHostEvents = 2 + kHostMaxChunks + kHostMaxColBlocks + kHostMaxChunks * kHostMaxColBlocks;
 struct HostPipe {
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t ev[2 + 2 * kHostMaxChunks] = {};
+    cudaEvent_t ev[kHostEvents] = {};
     std::mutex m;
 };
 std::map<int, HostPipe*> g_pipes;
@@ -84,12 +87,13 @@ gsr_status load_encoder() {
     return GSR_OK;
 }
 
-// Row-major fp16 matrix of `rows` x `cols` (cols contiguous) seen as a 2-D tensor map with
-// a box of box_cols x box_rows, 128-byte swizzle, zero fill outside the matrix.
+// Row-major fp16 matrix of `rows` x `cols` (cols contiguous, `ld` elements from one row to the
+// next; 0: dense, ld = cols) seen as a 2-D tensor map with a box of box_cols x box_rows, 128-byte
+// swizzle, zero fill outside the matrix (so a block of a wider matrix is clipped at its own edge).
 gsr_status encode_fp16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                          uint32_t box_cols, uint32_t box_rows) {
+                          uint32_t box_cols, uint32_t box_rows, uint64_t ld = 0) {
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {(ld ? ld : cols) * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
@@ -108,9 +112,9 @@ gsr_status encode_fp16_2d(CUtensorMap* map, const void* base, uint64_t rows, uin
 // consecutive chunks one after the other in shared memory, each box_k rows of 128 bytes
 // (the same layout as box_chunks separate 64 x box_k boxes), in one copy instruction.
 gsr_status encode_fp16_chunked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                               uint32_t box_rows, uint32_t box_chunks) {
+                               uint32_t box_rows, uint32_t box_chunks, uint64_t ld = 0) {
     cuuint64_t dims[3] = {64, rows, cols / 64};
-    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint64_t strides[2] = {(ld ? ld : cols) * 2, 128};
     cuuint32_t box[3] = {64, box_rows, box_chunks};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
@@ -316,9 +320,11 @@ struct Epi {
     const __half* bias;
 };
 
+// ldb, ldc: row strides (elements) of B and C when they are column blocks of wider matrices;
+// 0 for dense ones.
 gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
-                    const Epi& ep,
-                     cudaStream_t stream, int dev, const DeviceInfo& info) {
+                     const Epi& ep, cudaStream_t stream, int dev, const DeviceInfo& info,
+                     int64_t ldb = 0, int64_t ldc = 0) {
     StreamState st;
     gsr_status s = stream_state(dev, stream, 0, 0, &st);
     if (s != GSR_OK) return s;
@@ -334,8 +340,8 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
 
     CUtensorMap tmA, tmB, tmC;
     if ((s = encode_fp16_2d(&tmA, A, M, K, 64, 128)) != GSR_OK) return s;
-    if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) return s;
-    if ((s = encode_fp16_2d(&tmC, C, M, N, 64, 128)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64, ldb)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmC, C, M, N, 64, 128, ldc)) != GSR_OK) return s;
 
     gsr::TiledParams p;
     p.M = M;
@@ -362,8 +368,8 @@ gsr_status run_tiled(const void* A, const void* B, void* C, int M, int N, int K,
 }
 
 gsr_status run_pair(int bn, const void* A, const void* B, void* C, int M, int N, int K, float alpha,
-                    const Epi& ep,
-                    cudaStream_t stream, int dev, const DeviceInfo& info) {
+                    const Epi& ep, cudaStream_t stream, int dev, const DeviceInfo& info,
+                    int64_t ldb = 0, int64_t ldc = 0) {
     StreamState st;
     gsr_status s = stream_state(dev, stream, 0, 0, &st);
     if (s != GSR_OK) return s;
@@ -377,11 +383,11 @@ gsr_status run_pair(int bn, const void* A, const void* B, void* C, int M, int N,
     const int box_chunks = (bn == 256 && num_full == num_tiles) ? 2 : 1;
     if ((s = encode_fp16_2d(&tmA, A, M, K, 64, 128)) != GSR_OK) return s;
     if (chunked) {
-        if ((s = encode_fp16_chunked(&tmB, B, K, N, 64, box_chunks)) != GSR_OK) return s;
-    } else if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64)) != GSR_OK) {
+        if ((s = encode_fp16_chunked(&tmB, B, K, N, 64, box_chunks, ldb)) != GSR_OK) return s;
+    } else if ((s = encode_fp16_2d(&tmB, B, K, N, 64, 64, ldb)) != GSR_OK) {
         return s;
     }
-    if ((s = encode_fp16_2d(&tmC, C, M, N, 64, 128)) != GSR_OK) return s;
+    if ((s = encode_fp16_2d(&tmC, C, M, N, 64, 128, ldc)) != GSR_OK) return s;
     gsr::TiledParams p;
     p.b_chunked = chunked ? 1 : 0;
     p.M = M;
@@ -473,6 +479,27 @@ gsr_status gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N
     return run_tiled(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
 }
 
+// One block of the pipelined host path: M rows of A (dense, K wide) times N columns of B into
+// the same columns of C, B and C keeping the row strides ldb and ldc of the whole matrices
+// (validated whole by the caller).  A block always has more than 64 rows: the small-M kernel,
+// which writes C without a tensor map, never runs one.
+gsr_status gemm_block(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                      int64_t ldb, int64_t ldc, float alpha, CUstream_st* stream) {
+    int dev = 0;
+    DeviceInfo info;
+    gsr_status s = device_info(&dev, &info);
+    if (s != GSR_OK) return s;
+    if ((s = load_encoder()) != GSR_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Epi ep{gsr::kEpiScaleRelu, nullptr};
+    const int path = choose_path(M, N, info.num_sms);
+    if (path == 1) return GSR_ERR_INVALID_ARG;
+    if (path == 2 || path == 3)
+        return run_pair(path == 3 ? 128 : 256, A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info,
+                        ldb, ldc);
+    return run_tiled(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info, ldb, ldc);
+}
+
 }  // namespace
 
 extern "C" {
@@ -519,6 +546,26 @@ int host_chunk_rows(int64_t M, int64_t N, int64_t K) {
     return (int)rows;
 }
 
+// Columns per block of B and C when they are split into j blocks: whole 256-column pair tiles.
+int64_t host_block_cols(int64_t N, int j) { return ((N + j - 1) / j + 255) / 256 * 256; }
+
+// Column blocks of the pipelined host path.  Where C (copied back) outweighs A and B (copied
+// in), the copy back bounds the call, and with B sent whole it cannot start before all of B and
+// the first rows of A have landed (0.65 of 3.3 ms on 16384 x 14336 x 4096).  Split into column
+// blocks, the first block of C goes back once the first rows of A and the first block of B are
+// in.  Each block keeps at least a wave of 256 x 256 pair tiles per row chunk (fewer would leave
+// SMs idle in every block's product); at most kHostMaxColBlocks blocks.
+int host_col_blocks(int64_t M, int64_t N, int64_t K, int rows, int num_sms) {
+    if (rows == 0 || M * N <= M * K + K * N) return 1;
+    int best = 1;
+    for (int j = 2; j <= kHostMaxColBlocks; ++j) {
+        const int64_t cols = host_block_cols(N, j);
+        if ((N + cols - 1) / cols != j) continue;
+        if (((rows + 255) / 256) * (cols / 256) >= num_sms / 2) best = j;
+    }
+    return best;
+}
+
 gsr_status host_pipe(int dev, HostPipe** out) {
     std::lock_guard<std::mutex> lock(g_mu);
     HostPipe*& hp = g_pipes[dev];
@@ -526,7 +573,7 @@ gsr_status host_pipe(int dev, HostPipe** out) {
         HostPipe* fresh = new HostPipe();
         cudaError_t e = cudaStreamCreateWithFlags(&fresh->h2d, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&fresh->d2h, cudaStreamNonBlocking);
-        for (int i = 0; e == cudaSuccess && i < 2 + 2 * kHostMaxChunks; ++i)
+        for (int i = 0; e == cudaSuccess && i < kHostEvents; ++i)
             e = cudaEventCreateWithFlags(&fresh->ev[i], cudaEventDisableTiming);
         if (e != cudaSuccess) {
             for (cudaEvent_t ev : fresh->ev)
@@ -546,12 +593,14 @@ gsr_status host_pipe(int dev, HostPipe** out) {
 
 extern "C" {
 
-// The host path overlaps its three parts: B goes over first, then the rows of A in chunks;
-// the product of chunk r runs as soon as its rows have landed, and its rows of C go back
-// while later chunks are copied in and multiplied.  Copies in each direction run on a
-// library stream of their own (host->device and device->host use separate copy engines),
-// the products on the caller's stream, joined by events: the whole call still behaves as
-// one operation on `stream`.  Small problems run the three parts one after the other.
+// The host path overlaps its three parts.  A goes over in row chunks and B whole, or, where C
+// is the larger transfer, in column blocks (host_col_blocks); the product of each (row chunk,
+// column block) runs as soon as both have landed, and that block of C goes back (a strided
+// copy when there are column blocks) while later ones are copied in and multiplied.  Copies in
+// each direction run on a library stream of their own (host->device and device->host use
+// separate copy engines), the products on the caller's stream, joined by events: the whole
+// call still behaves as one operation on `stream`.  Small problems run the three parts one
+// after the other.
 gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* dA, void* dB,
                                 void* dC, int64_t M, int64_t N, int64_t K, float alpha,
                                 CUstream_st* stream) {
@@ -580,39 +629,76 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
     HostPipe* hp = nullptr;
     if ((s = host_pipe(dev, &hp)) != GSR_OK) return s;
     std::lock_guard<std::mutex> lock(hp->m);
-    const int nch = (int)((M + rows - 1) / rows);
+    // Row chunks [m0[r], m0[r + 1]) (a last one of 64 rows or fewer joins the one before it, so
+    // no product is a small-M one) and column blocks of `cols` columns of B and C.
+    int64_t m0[kHostMaxChunks + 1];
+    int nch = 0;
+    for (int64_t m = 0; m < M && nch < kHostMaxChunks; m += rows) m0[nch++] = m;
+    if (nch > 1 && M - m0[nch - 1] <= 64) --nch;
+    m0[nch] = M;
+    const int nblk = host_col_blocks(M, N, K, rows, info.num_sms);
+    const int64_t cols = nblk > 1 ? host_block_cols(N, nblk) : N;
     cudaEvent_t start = hp->ev[0], done = hp->ev[1];
     auto ev_a = [&](int r) { return hp->ev[2 + r]; };
-    auto ev_c = [&](int r) { return hp->ev[2 + kHostMaxChunks + r]; };
+    auto ev_b = [&](int j) { return hp->ev[2 + kHostMaxChunks + j]; };
+    auto ev_c = [&](int r, int j) { return hp->ev[2 + kHostMaxChunks + kHostMaxColBlocks + r * kHostMaxColBlocks + j]; };
     const char* a_h = static_cast<const char*>(hA);
+    const char* b_h = static_cast<const char*>(hB);
     char* a_d = static_cast<char*>(dA);
+    char* b_d = static_cast<char*>(dB);
     char* c_h = static_cast<char*>(hC);
     char* c_d = static_cast<char*>(dC);
-    // host -> device: after everything already queued on the caller's stream
+    const size_t row_b = (size_t)N * 2;   // bytes from one row of B or C to the next
+    auto copy_a = [&](int r) {
+        const size_t off = (size_t)m0[r] * K * 2, bytes = (size_t)(m0[r + 1] - m0[r]) * K * 2;
+        cudaError_t err = cudaMemcpyAsync(a_d + off, a_h + off, bytes, cudaMemcpyHostToDevice, hp->h2d);
+        return err == cudaSuccess ? cudaEventRecord(ev_a(r), hp->h2d) : err;
+    };
+    auto copy_b = [&](int j) {
+        const int64_t n0 = j * cols, nj = (N - n0 < cols) ? N - n0 : cols;
+        cudaError_t err = nblk == 1 ? cudaMemcpyAsync(b_d, b_h, (size_t)K * row_b, cudaMemcpyHostToDevice, hp->h2d)
+                                    : cudaMemcpy2DAsync(b_d + n0 * 2, row_b, b_h + n0 * 2, row_b, (size_t)nj * 2,
+                                                        (size_t)K, cudaMemcpyHostToDevice, hp->h2d);
+        return err == cudaSuccess ? cudaEventRecord(ev_b(j), hp->h2d) : err;
+    };
+    // host -> device, after everything already queued on the caller's stream: the first rows of
+    // A and the first block of B, then the other rows of A (each one lets a block of the first
+    // column go), then the other blocks of B
     gsr_status result = GSR_OK;
     if ((e = cudaEventRecord(start, st)) != cudaSuccess) return cuda_fail(e);   // nothing queued yet
-    if ((e = cudaStreamWaitEvent(hp->h2d, start, 0)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dB, hB, (size_t)K * N * 2, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess)
+    if ((e = cudaStreamWaitEvent(hp->h2d, start, 0)) != cudaSuccess || (e = copy_a(0)) != cudaSuccess ||
+        (e = copy_b(0)) != cudaSuccess)
         result = cuda_fail(e);
-    for (int r = 0; r < nch && result == GSR_OK; ++r) {
-        const int64_t m0 = (int64_t)r * rows, mr = (M - m0 < rows) ? M - m0 : rows;
-        if ((e = cudaMemcpyAsync(a_d + m0 * K * 2, a_h + m0 * K * 2, (size_t)(mr * K * 2), cudaMemcpyHostToDevice,
-                                 hp->h2d)) != cudaSuccess ||
-            (e = cudaEventRecord(ev_a(r), hp->h2d)) != cudaSuccess)
-            result = cuda_fail(e);
-    }
-    for (int r = 0; r < nch && result == GSR_OK; ++r) {
-        const int64_t m0 = (int64_t)r * rows, mr = (M - m0 < rows) ? M - m0 : rows;
-        if ((e = cudaStreamWaitEvent(st, ev_a(r), 0)) != cudaSuccess) {
+    for (int r = 1; r < nch && result == GSR_OK; ++r)
+        if ((e = copy_a(r)) != cudaSuccess) result = cuda_fail(e);
+    for (int j = 1; j < nblk && result == GSR_OK; ++j)
+        if ((e = copy_b(j)) != cudaSuccess) result = cuda_fail(e);
+    // the products on the caller's stream, block column by block column, each block of C going
+    // back on the copy stream as soon as it is written
+    for (int j = 0; j < nblk && result == GSR_OK; ++j) {
+        const int64_t n0 = j * cols, nj = (N - n0 < cols) ? N - n0 : cols;
+        if ((e = cudaStreamWaitEvent(st, ev_b(j), 0)) != cudaSuccess) {
             result = cuda_fail(e);
             break;
         }
-        if ((result = gemm_scale_relu(a_d + m0 * K * 2, dB, c_d + m0 * N * 2, mr, N, K, alpha, stream)) != GSR_OK)
-            break;
-        if ((e = cudaEventRecord(ev_c(r), st)) != cudaSuccess || (e = cudaStreamWaitEvent(hp->d2h, ev_c(r), 0)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(c_h + m0 * N * 2, c_d + m0 * N * 2, (size_t)(mr * N * 2), cudaMemcpyDeviceToHost,
-                                 hp->d2h)) != cudaSuccess)
-            result = cuda_fail(e);
+        for (int r = 0; r < nch && result == GSR_OK; ++r) {
+            const int64_t mr = m0[r + 1] - m0[r];
+            const size_t c_off = (size_t)m0[r] * row_b + (size_t)n0 * 2;
+            if (j == 0 && (e = cudaStreamWaitEvent(st, ev_a(r), 0)) != cudaSuccess) {
+                result = cuda_fail(e);
+                break;
+            }
+            if ((result = gemm_block(a_d + (size_t)m0[r] * K * 2, b_d + n0 * 2, c_d + c_off, mr, nj, K, N, N,
+                                     alpha, stream)) != GSR_OK)
+                break;
+            if ((e = cudaEventRecord(ev_c(r, j), st)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(hp->d2h, ev_c(r, j), 0)) != cudaSuccess ||
+                (e = nblk == 1 ? cudaMemcpyAsync(c_h + c_off, c_d + c_off, (size_t)mr * row_b, cudaMemcpyDeviceToHost,
+                                                 hp->d2h)
+                               : cudaMemcpy2DAsync(c_h + c_off, row_b, c_d + c_off, row_b, (size_t)nj * 2,
+                                                   (size_t)mr, cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess)
+                result = cuda_fail(e);
+        }
     }
     // The caller's stream continues only after both copy streams (the last copy back, and on a
     // failure whatever copies in were queued), so nothing of this call is left running unordered.

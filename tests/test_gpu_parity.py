@@ -326,10 +326,17 @@ def test_host_entry_point_round_trip():
 @pytest.mark.parametrize("M,N,K,chunk", [(1200, 1000, 1024, 0),         # below the threshold: one piece
                                           (2000, 3000, 1000, 1024),      # 1024 rows + 976
                                           (2500, 4096, 4096, 512),       # 4 x 512 rows + 452
-                                          (4096, 4096, 4096, 512)])      # 8 x 512 rows
+                                          (4096, 4096, 4096, 512),       # 8 x 512 rows
+                                          # C larger than A and B: B and C in 3 column blocks of
+                                          # 5632, 5632 and 5120 columns, strided copies both ways
+                                          (8192, 16384, 512, 1024),
+                                          # the same with 7 x 1024 rows + 32 (joined to the 7th)
+                                          # and a last block of 5112 columns (not a multiple of 64)
+                                          (7200, 16376, 512, 1024)])
 def test_host_entry_point_in_chunks(M, N, K, chunk):
-    # Large enough for the pipelined host path: B first, A's rows in chunks, each chunk's
-    # product and copy back overlapping the next chunk's copy in.  Every row must arrive.
+    # Large enough for the pipelined host path: A's rows in chunks (and B and C in column
+    # blocks where C is the larger transfer), each block's product and copy back overlapping
+    # the copies in of later ones.  Every element must arrive.
     A, B = make_inputs(M, N, K, seed=M + K)
     hA, hB = A.pin_memory(), B.pin_memory()
     hC = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
