@@ -261,6 +261,15 @@ void gsr_set_path_override(int path);
  * measurements. */
 void gsr_set_raster_group(int group);
 
+/* Split-K of the small-M kernel (process-wide): each 128-column tile's K is cut
+ * into `slabs` slabs of whole 64-wide k-blocks (at most one slab per k-block), run
+ * as separate work items and summed in slab order (deterministic for a given
+ * `slabs`).  0 restores the default, as many slabs as fill the SMs once.  The
+ * split-K knob of the aikraft.ru TileLang tutorial survey's "Knobs" section (3);
+ * for tuning and measurements.  gemm_scale_relu_noalloc ignores it (its fixed
+ * scratch is sized for the default split). */
+void gsr_set_split_k(int slabs);
+
 /* Upper bound, in nanoseconds, on every wait inside the kernels (default 1 s).
  * A wait that runs out records an error (see gsr_device_status) and the kernel
  * exits early, leaving C incomplete. */

@@ -11,7 +11,7 @@ from .binding import (KERNEL_PAIR, KERNEL_PAIR_128, KERNEL_SKINNY, KERNEL_TILED,
                       gemm_bias_gelu_ptr,
                       gemm_scale, gemm_scale_relu, gemm_scale_relu_host,
                       gemm_scale_relu_host_ptr, gemm_scale_relu_ptr, last_cuda_error, lib,
-                      library_path, select_path, set_path_override, set_raster_group, set_test_flags,
+                      library_path, select_path, set_path_override, set_raster_group, set_split_k, set_test_flags,
                       set_wait_timeout_ns, shutdown, status_string, version)
 from ._build import build
 
@@ -20,6 +20,6 @@ __all__ = [
     "Status", "build", "device_status", "flash_attention_fwd", "gemm_bias_gelu", "gemm_bias_gelu_ptr", "gemm_scale",
     "gemm_scale_relu", "gemm_scale_relu_host",
     "gemm_scale_relu_host_ptr", "gemm_scale_relu_ptr", "last_cuda_error", "lib", "library_path",
-    "release_stream", "select_path", "set_path_override", "set_raster_group", "set_test_flags", "set_wait_timeout_ns", "shutdown",
+    "release_stream", "select_path", "set_path_override", "set_raster_group", "set_split_k", "set_test_flags", "set_wait_timeout_ns", "shutdown",
     "status_string", "version",
 ]

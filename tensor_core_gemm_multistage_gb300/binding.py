@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.gsr_set_wait_timeout_ns.argtypes = [u64]
         L.gsr_set_raster_group.restype = None
         L.gsr_set_raster_group.argtypes = [i32]
+        L.gsr_set_split_k.restype = None
+        L.gsr_set_split_k.argtypes = [i32]
         L.gsr_set_test_flags.restype = None
         L.gsr_set_test_flags.argtypes = [u32]
         L.gsr_last_cuda_error.restype = i32
@@ -129,6 +131,10 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def set_raster_group(group: int) -> None:
     lib().gsr_set_raster_group(int(group))
+
+
+def set_split_k(slabs: int) -> None:
+    lib().gsr_set_split_k(int(slabs))
 
 
 def set_test_flags(flags: int) -> None:

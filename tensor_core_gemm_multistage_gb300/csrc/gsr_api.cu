@@ -26,6 +26,7 @@ std::atomic<int> g_path_override{0};
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<uint32_t> g_test_flags{0};
 std::atomic<int> g_raster_group{0};   // 0: each kernel's default grouping
+std::atomic<int> g_split_k{0};        // 0: the small-M kernel's own slab count
 
 constexpr int kSkinnyMaxM = 64;
 constexpr int kGroupM = 16;
@@ -424,6 +425,11 @@ gsr_status run_skinny(const void* A, const void* B, void* C, int M, int N, int K
     const int kbpt = (K + 63) / 64;
     int S = 1, P = 1;
     gsr::skinny_split(n_tiles, kbpt, info.num_sms, &S, &P);
+    if (const int o = g_split_k.load(std::memory_order_relaxed)) {   // every slab keeps a k-block
+        S = o < kbpt ? o : kbpt;
+        const long long items = (long long)n_tiles * S;
+        P = (int)(items < info.num_sms ? items : info.num_sms);
+    }
 
     StreamState st;
     const size_t partial_floats = S > 1 ? (size_t)n_tiles * S * mp * 128 : 0;
@@ -918,6 +924,8 @@ void gsr_set_wait_timeout_ns(uint64_t ns) {
 }
 
 void gsr_set_raster_group(int group) { g_raster_group.store(group > 0 ? group : 0, std::memory_order_relaxed); }
+
+void gsr_set_split_k(int slabs) { g_split_k.store(slabs > 0 ? slabs : 0, std::memory_order_relaxed); }
 
 void gsr_set_test_flags(uint32_t flags) { g_test_flags.store(flags, std::memory_order_relaxed); }
 

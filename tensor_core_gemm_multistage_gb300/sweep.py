@@ -12,6 +12,8 @@ static_assert), so the runtime knobs are:
   l2       the CTA-pair kernels' L2 handling: "default" (serpentine K order across waves,
            evict-last A and B, evict-first C stores), "k_forward" (every wave walks K forward),
            "b_evict_first" (B copies marked evict-first)
+  split    the small-M kernel's split-K: slabs per 128-column tile (gsr_set_split_k; 0: its
+           own choice, as many slabs as fill the SMs once)
 
     python -m tensor_core_gemm_multistage_gb300.sweep --M 8192 --N 8192 --K 8192
 
@@ -40,12 +42,13 @@ KERNELS = {"tiled_128x256": gsr.PATH_TILED_256, "tiled_128x128": gsr.PATH_TILED_
            "tiled_128x64": gsr.PATH_TILED_64,
            "pair_256x256": gsr.PATH_PAIR, "pair_256x128": gsr.PATH_PAIR_128, "small_m": gsr.PATH_SKINNY}
 RASTERS = (0, 4, 16)     # 0: the kernel's default grouping
+SPLITS = (0, 1, 2, 4, 8, 16, 32)   # small-M slabs per tile; 0: the kernel's default
 NO_3D_B = 2              # test flag bit 1
 L2_MODES = {"default": 0, "k_forward": 4, "b_evict_first": 32}   # test flag bits 2 and 5
 
 
 def candidates(M: int, N: int, K: int):
-    """Every (kernel, raster, b_copy) combination that is valid for this shape."""
+    """Every (kernel, raster, b_copy, l2, split) combination that is valid for this shape."""
     out = []
     for name, path in KERNELS.items():
         if name == "small_m" and M > 64:
@@ -53,10 +56,13 @@ def candidates(M: int, N: int, K: int):
         rasters = (0,) if name == "small_m" else RASTERS
         copies = ("3d", "2d") if (name.startswith("pair_") and N % 64 == 0) else ("default",)
         l2s = tuple(L2_MODES) if name.startswith("pair_") else ("default",)
+        splits = tuple(x for x in SPLITS if x <= (K + 63) // 64) if name == "small_m" else (0,)
         for r in rasters:
             for c in copies:
                 for l2 in l2s:
-                    out.append({"kernel": name, "path": path, "raster": r, "b_copy": c, "l2": l2})
+                    for sp in splits:
+                        out.append({"kernel": name, "path": path, "raster": r, "b_copy": c, "l2": l2,
+                                    "split": sp})
     return out
 
 
@@ -65,6 +71,7 @@ def time_config(cfg, A, B, C, alpha, warmup=5, iters=30):
     gsr.set_path_override(cfg["path"])
     gsr.set_raster_group(cfg["raster"])
     gsr.set_test_flags((NO_3D_B if cfg["b_copy"] == "2d" else 0) | L2_MODES[cfg.get("l2", "default")])
+    gsr.set_split_k(cfg.get("split", 0))
     try:
         for _ in range(warmup):
             gsr.gemm_scale_relu(A, B, C, alpha)
@@ -84,6 +91,7 @@ def time_config(cfg, A, B, C, alpha, warmup=5, iters=30):
         gsr.set_path_override(gsr.PATH_AUTO)
         gsr.set_raster_group(0)
         gsr.set_test_flags(0)
+        gsr.set_split_k(0)
 
 
 def sweep(M: int, N: int, K: int, alpha: float = 0.5, warmup: int = 5, iters: int = 30, seed=0,

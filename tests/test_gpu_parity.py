@@ -133,6 +133,26 @@ def test_small_m_path(M, N, K):
     parity(M, N, K, 0.75, path=gsr.PATH_SKINNY, seed=M * N + K, b_scaled=True)
 
 
+@pytest.mark.parametrize("M,N,K,slabs", [(16, 1024, 2048, 1),     # no split: one item per tile
+                                          (16, 1024, 2048, 3),     # 32 k-blocks in slabs of 10/11/11
+                                          (40, 1000, 1000, 16),    # 16 k-blocks, one per slab
+                                          (40, 1000, 1000, 99),    # asked for more: clamped to 16
+                                          (64, 4096, 8192, 64)])   # more slabs than the default 4
+def test_small_m_split_override(M, N, K, slabs):
+    # gsr_set_split_k: any slab count sums every k-block once (slab order is fixed, so a second
+    # call gives the same bytes); the per-stream workspace grows for more slabs than the default
+    A, B = make_inputs(M, N, K, seed=M + slabs, b_std_inv_sqrt_k=True)
+    gsr.set_split_k(slabs)
+    try:
+        C = run_gpu(A, B, 0.5, gsr.PATH_SKINNY)
+        C2 = run_gpu(A, B, 0.5, gsr.PATH_SKINNY)
+    finally:
+        gsr.set_split_k(0)
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, return_pre=True)
+    check(C, ref, z, "split %d" % slabs)
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+
+
 @pytest.mark.parametrize("name", ["square1024", "ragged2000x3000x1000"])
 @pytest.mark.parametrize("path", [gsr.PATH_TILED_128, gsr.PATH_TILED_64, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
 def test_small_workloads_on_each_tiled_kernel(name, path):

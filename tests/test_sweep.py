@@ -18,6 +18,10 @@ def test_candidates_respect_each_kernels_limits():
     assert "small_m" in {c["kernel"] for c in small}
     assert {c["b_copy"] for c in small} == {"default"}
     assert all(c["raster"] == 0 for c in small if c["kernel"] == "small_m")
+    # split-K only for the small-M kernel, never more slabs than 64-wide k-blocks (4096 / 64)
+    assert {c["split"] for c in small if c["kernel"] == "small_m"} == set(sweep.SPLITS)
+    assert {c["split"] for c in small if c["kernel"] != "small_m"} == {0}
+    assert {c["split"] for c in sweep.candidates(16, 1024, 256) if c["kernel"] == "small_m"} == {0, 1, 2, 4}
 
 
 @pytest.mark.gpu
