@@ -238,10 +238,13 @@ gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
 gsr_status gsr_release_stream(struct CUstream_st* stream);
 
 /* Kernel the library would run for these sizes on the current device: 0 = tiled
- * (one CTA per 128-row tile), 1 = small-M, 2 = tiled on CTA pairs with 256 x 256
- * tiles (chosen when there is at least one full wave of such tiles), 3 = tiled on
- * CTA pairs with 256 x 128 tiles (instead of 2 when 256-wide tiles would leave the
- * last wave badly filled). */
+ * (one CTA per 128-row tile, 128 x 256 or 128 x 128 tiles, whichever needs fewer
+ * waves with a wave of the wider ones counted as 1.45), 1 = small-M (M <= 64),
+ * 2 = tiled on CTA pairs with 256 x 256 tiles (chosen when there is at least one
+ * full wave of such tiles), 3 = tiled on CTA pairs with 256 x 128 tiles (instead
+ * of 2 where a wave of them, counted as 0.68 of a wide wave, finishes the work at
+ * least 5 % sooner: in practice N of about 128, where a 256-wide tile is half
+ * empty).  The constants come from measured sweeps on GB300. */
 int gsr_select_path(int64_t M, int64_t N, int64_t K);
 
 /* Forces a path for later calls (process-wide): 0 = automatic (default),
