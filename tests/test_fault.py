@@ -101,6 +101,43 @@ def test_small_m_timeout_needs_no_status_call_to_recover():
     assert gsr.device_status() == (gsr.Status.OK, 0)
 
 
+def test_host_entry_point_blocks_time_out_and_recover():
+    # The pipelined host path with B and C in column blocks (3 blocks x 8 row chunks, 24 pair
+    # launches): every launch loses its first copy and gives up.  The call still completes (the
+    # copy streams are joined back to the caller's stream), the timeout is reported on that
+    # stream, and the next call on the same buffers is correct everywhere.
+    M, N, K = 8192, 16384, 512
+    A, B = make_inputs(M, N, K, seed=25)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    dev = torch.device("cuda", 0)
+    dA = torch.empty(M, K, dtype=torch.float16, device=dev)
+    dB = torch.empty(K, N, dtype=torch.float16, device=dev)
+    dC = torch.empty(M, N, dtype=torch.float16, device=dev)
+    stream = torch.cuda.Stream()
+    gsr.set_wait_timeout_ns(20_000_000)        # 20 ms
+    gsr.set_test_flags(1)
+    try:
+        gsr.gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, 0.5, stream=stream)
+        stream.synchronize()
+        status, code = gsr.device_status(stream)
+    finally:
+        gsr.set_test_flags(0)
+        gsr.set_wait_timeout_ns(1_000_000_000)
+    assert status == gsr.Status.ERR_DEVICE_TIMEOUT and code & 0xF00 == 0x100, hex(code)
+    hC.fill_(float("nan"))
+    gsr.gemm_scale_relu_host(hA, hB, hC, dA, dB, dC, 0.5, stream=stream)
+    stream.synchronize()
+    assert gsr.device_status(stream) == (gsr.Status.OK, 0)
+    C = hC.clone()
+    assert not torch.isnan(C).any()
+    rows = np.unique(np.concatenate([np.arange(0, M, 1024), np.arange(1023, M, 1024),
+                                     np.random.default_rng(5).integers(0, M, 64)]))
+    ref = oracle.gemm_scale_relu(A, B, 0.5, rows=rows).astype(np.float64)
+    got = C[rows].numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+
+
 def test_release_stream_frees_and_the_stream_stays_usable():
     dev = torch.device("cuda", 0)
     s = torch.cuda.Stream(dev)
