@@ -408,6 +408,39 @@ def test_pair_kernel_l2_switches(flags):
     check(C if rows is None else C[rows], ref, z, "pair flags %d" % flags)
 
 
+# ---------------------------------------------------------------------------- random shapes
+
+def _random_shapes(n, seed):
+    # seeded shapes for the automatic path: every kernel and tile width the host can choose,
+    # ragged in M, N and K (N, K multiples of 8 as the boundary requires)
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.choice([rng.integers(1, 65), rng.integers(65, 1600)]))
+        N = int(rng.integers(1, 190)) * 8
+        K = int(rng.integers(1, 129)) * 8
+        out.append((M, N, K, float(rng.choice([0.5, 1.0, -0.75, 1.25]))))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,alpha", _random_shapes(24, 2026))
+def test_random_shapes_auto(M, N, K, alpha):
+    parity(M, N, K, alpha, seed=M + 3 * N + 7 * K, b_scaled=True)
+
+
+def _random_large_shapes(n, seed):
+    # at least a wave of 256 x 256 pair tiles: the CTA-pair kernels (whole tiles, half-width
+    # last waves, 256- or 128-wide tiles), checked on sampled rows
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(2300, 6001)), int(rng.integers(16, 751)) * 8, int(rng.integers(8, 129)) * 8,
+             float(rng.choice([0.5, 1.0, -0.75]))) for _ in range(n)]
+
+
+@pytest.mark.parametrize("M,N,K,alpha", _random_large_shapes(8, 2027))
+def test_random_large_shapes_auto(M, N, K, alpha):
+    parity(M, N, K, alpha, seed=M + N + K, b_scaled=True, rows=sample_rows(M))
+
+
 # ---------------------------------------------------------------------------- large sizes
 
 def test_a_million_rows():
