@@ -189,3 +189,21 @@ def test_two_streams_at_once_keep_their_own_work_counters():
         x = o.cpu().numpy().astype(np.float64)
         assert not np.isnan(x).any()
         assert np.all(np.abs(x - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+
+
+def _random_attention_cases(n, seed):
+    # seeded (B, H, Sq, Skv, D, causal, scale): ragged lengths on both sides, Sq above and below
+    # Skv (causal diagonals offset either way), both head sizes, default and explicit scales
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 5))
+        Sq, Skv = int(rng.integers(1, 700)), int(rng.integers(1, 900))
+        D = int(rng.choice([64, 128]))
+        out.append((B, H, Sq, Skv, D, bool(rng.integers(0, 2)), float(rng.choice([0.0, 0.05, 0.2]))))
+    return out
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,D,causal,scale", _random_attention_cases(16, 2028))
+def test_random_attention_cases(B, H, Sq, Skv, D, causal, scale):
+    check(*inputs(B, H, Sq, Skv, D, seed=B + H + Sq + Skv + D), causal=causal, scale=scale)
