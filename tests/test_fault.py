@@ -28,12 +28,15 @@ def built():
     gsr.set_path_override(gsr.PATH_AUTO)
 
 
+# The skipped fill turns into a timeout once the producer has to wait for the stage it never
+# filled, so each CTA's work must run past its ring of stages (on CTA pairs K = 4096: 32 stages
+# per tile against a ring of 3 or 4).
 @pytest.mark.parametrize("M,N,K,path,kernel,flags", [(512, 1024, 1024, gsr.PATH_TILED, 0x100, 1),
-                                                     (1024, 2048, 1024, gsr.PATH_PAIR, 0x100, 1),
-                                                     (1024, 2048, 1024, gsr.PATH_PAIR_128, 0x100, 1),
+                                                     (1024, 2048, 4096, gsr.PATH_PAIR, 0x100, 1),
+                                                     (1024, 2048, 4096, gsr.PATH_PAIR_128, 0x100, 1),
                                                      # the first pair's second CTA skips its fill
-                                                     (1024, 2048, 1024, gsr.PATH_PAIR, 0x100, 16),
-                                                     (1024, 2048, 1024, gsr.PATH_PAIR_128, 0x100, 16),
+                                                     (1024, 2048, 4096, gsr.PATH_PAIR, 0x100, 16),
+                                                     (1024, 2048, 4096, gsr.PATH_PAIR_128, 0x100, 16),
                                                      (2000, 3000, 1000, gsr.PATH_PAIR, 0x100, 16),
                                                      (300, 512, 1024, gsr.PATH_TILED_64, 0x100, 1),
                                                      (16, 4096, 8192, gsr.PATH_SKINNY, 0x200, 1)])

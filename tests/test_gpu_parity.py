@@ -408,6 +408,27 @@ def test_pair_kernel_l2_switches(flags):
     check(C if rows is None else C[rows], ref, z, "pair flags %d" % flags)
 
 
+# ---------------------------------------------------------------------------- partial last waves
+
+@pytest.mark.parametrize("M,N,K,path,full", [
+    (2000, 3000, 1000, gsr.PATH_AUTO, True),    # 96 tiles: 76 whole, then 20 as 40 half-width units
+    (3000, 2600, 200, gsr.PATH_AUTO, True),     # 132 tiles: a last wave of 56 whole tiles, two stages each
+    (2560, 2560, 64, gsr.PATH_AUTO, True),      # 100 tiles, one stage each: 24 tiles as 48 halves
+    (1024, 2048, 1024, gsr.PATH_PAIR, True),    # 32 tiles, no full wave
+    (4096, 4096, 1024, gsr.PATH_AUTO, False),   # 256 tiles: 3 waves, then 28 tiles as 56 halves
+    (6144, 3072, 2048, gsr.PATH_AUTO, False)])  # 288 tiles: 3 waves, then 60 whole tiles
+def test_pair_partial_last_wave(M, N, K, path, full):
+    # Pair launches whose last wave is partial, with 1 to 16 stages per tile; a second call on
+    # the same inputs gives the same bytes (every output element is summed in one fixed order).
+    A, B = make_inputs(M, N, K, seed=M + N + K, b_std_inv_sqrt_k=True)
+    rows = None if full else sample_rows(M)
+    ref, z = oracle.gemm_scale_relu(A, B, 0.5, rows=rows, return_pre=True)
+    C = run_gpu(A, B, 0.5, path)
+    check(C if full else C[rows], ref, z, "last wave %dx%dx%d" % (M, N, K))
+    C2 = run_gpu(A, B, 0.5, path)
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+
+
 # ---------------------------------------------------------------------------- random shapes
 
 def _random_shapes(n, seed):
