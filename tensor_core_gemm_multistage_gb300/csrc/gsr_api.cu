@@ -2,9 +2,9 @@
 // per-(device, stream) state, and the launches.  See include/gsr.h for the contract.
 //
 // Nothing here computes any part of the operator; every step of C = ReLU(alpha * A.B)
-// runs in the kernels of gemm_tiled.cu and gemm_skinny.cu.  The one exception is
-// K == 0, where the empty sum makes every output ReLU(alpha * 0) = 0 and C is cleared
-// with cudaMemsetAsync.
+// runs in the kernels of gemm_tiled.cu, gemm_pair.cu and gemm_skinny.cu (attention in
+// attention_fwd.cu).  The one exception is K == 0, where the empty sum makes every output
+// ReLU(alpha * 0) = 0 and C is cleared with cudaMemsetAsync (GELU(bias) by a fill kernel).
 #include <cudaTypedefs.h>
 
 #include <atomic>
