@@ -15,7 +15,11 @@ Prints ONE JSON line (rank 0).  Besides the timing it carries:
   e2e           the same metric through gemm_scale_relu_host: pinned host A, B copied in
                 and C copied out inside the timed region, every step;
   cpu_baseline  the fp64 CPU oracle timed on this host on a bounded sample of rows;
-  clocks        SM clocks and throttle reasons sampled by nvidia-smi during the run.
+  clocks        SM clocks and throttle reasons sampled by nvidia-smi during the timed region
+                (and, under median5_window, during the longer repeats that follow it);
+  median5       the median over 5 repeats of >= 100 back-to-back calls after the timed region;
+  per_config    the other four GEMM configurations, each timed the same way in the same run,
+                with its own roofline and CPU-oracle time.
 With --impl reference the line times the oracle itself (the CPU reference arm).
 N > 1 (torchrun): every rank runs its own full copy of the workload (replicas, weak
 scaling); the time is the max over ranks and the value the sum of all ranks' work.
