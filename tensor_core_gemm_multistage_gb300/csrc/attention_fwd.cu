@@ -44,12 +44,16 @@ struct AttnCfg {
     static constexpr int KV_BYTES = BKV * D * 2;
     static constexpr int SM_THREADS = 128 * NQ;       // softmax threads
     static constexpr int NUM_THREADS = 64 + SM_THREADS;
+    // Q buffers: at D = 64 a second set (32 KB) fits, so the next item's Q loads while the
+    // current item still reads its own; at D = 128 there is no room (one set, reloaded once the
+    // last Q K^T products of an item have read it)
+    static constexpr int QBUF = D == 64 ? 2 : 1;
     // ring of 2 entries; entry e holds K_e and V_{e-1}, the two tiles step e consumes
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
+    static constexpr int OFF_K = OFF_Q + QBUF * NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
-    static constexpr int NUM_BARS = 17;
+    static constexpr int NUM_BARS = 17 + 2 * (QBUF - 1);
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     // no alignment slack: the window is declared 1024-byte aligned and the kernel checks it
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -82,9 +86,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t sb = smem_u32(smem);
 
     // barriers: 0 qfull | 1 qfree | 2+s full | 4+s empty | 6+q sfull | 8+q pfull | 10+q odone |
-    // 12+i item published | 14+i item read | 16 drain
+    // 12+i item published | 14+i item read | 16 drain | 17 qfull, 18 qfree of the second Q set
     auto bar = [&](int i) { return sb + Cfg::OFF_BAR + 8u * i; };
-    const uint32_t qfull = bar(0), qfree = bar(1), drain = bar(16);
+    const uint32_t drain = bar(16);
+    auto qfull = [&](int b) { return bar(b == 0 ? 0 : 17); };
+    auto qfree = [&](int b) { return bar(b == 0 ? 1 : 18); };
     auto full = [&](int s) { return bar(2 + s); };
     auto empty = [&](int s) { return bar(4 + s); };
     auto sfull = [&](int q) { return bar(6 + q); };
@@ -129,8 +135,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(qfull, 1);
-        mbar_init(qfree, 1);
+        for (int b = 0; b < Cfg::QBUF; ++b) {
+            mbar_init(qfull(b), 1);
+            mbar_init(qfree(b), 1);
+        }
         for (int s = 0; s < 2; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_last();   // K and V are read by every query block
             uint32_t n_pub = 0, n_q = 0, g = 0;            // items published, Q loads, ring entries
-            bool q_armed = false;
+            int last_q0 = -1, last_q1 = -1;                 // Q load number last armed, per set
             uint32_t ring_armed = 0, ring_parity = 0;
             bool drop_q = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
             while (true) {
@@ -185,18 +193,23 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 if (item < 0) break;
                 const Item it = decode(item);
                 if (it.nkv_max == 0) continue;       // no keys: O = 0 needs no copies
-                if (n_q > 0 && !w.wait(qfree, (n_q - 1) & 1u, kDevErrProducerEmpty)) break;
+                // Q set n_q % QBUF: free once the item that last used it has read it
+                const int qb = (int)(n_q % Cfg::QBUF);
+                if (n_q >= (uint32_t)Cfg::QBUF &&
+                    !w.wait(qfree(qb), ((n_q - Cfg::QBUF) / Cfg::QBUF) & 1u, kDevErrProducerEmpty))
+                    break;
                 if (drop_q) {
                     drop_q = false;                  // test hook: this Q is never loaded
                 } else {
-                    mbar_arrive_expect_tx(qfull, NQ * Cfg::Q_BYTES);
+                    const uint32_t qbase = sb + Cfg::OFF_Q + qb * NQ * Cfg::Q_BYTES;
+                    mbar_arrive_expect_tx(qfull(qb), NQ * Cfg::Q_BYTES);
 #pragma unroll
                     for (int q = 0; q < NQ; ++q)
 #pragma unroll
                         for (int c = 0; c < Cfg::DCH; ++c)
-                            tma_load_3d(sb + Cfg::OFF_Q + q * Cfg::Q_BYTES + c * Cfg::CHUNK_BYTES, &tmQ, qfull,
+                            tma_load_3d(qbase + q * Cfg::Q_BYTES + c * Cfg::CHUNK_BYTES, &tmQ, qfull(qb),
                                         c * 64, it.q_base + q * Cfg::BQ, it.bh, pol);
-                    q_armed = true;
+                    (qb == 0 ? last_q0 : last_q1) = (int)n_q;
                 }
                 ++n_q;
                 bool ok = true;
@@ -236,7 +249,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 atomicExch(p.work + 1, 0);
             }
             // every copy started must land before the CTA may exit
-            if (q_armed) w.drain(qfull, (n_q - 1) & 1u);
+            if (last_q0 >= 0) w.drain(qfull(0), (uint32_t)(last_q0 / Cfg::QBUF) & 1u);
+            if (last_q1 >= 0) w.drain(qfull(1), (uint32_t)(last_q1 / Cfg::QBUF) & 1u);
             for (int s = 0; s < 2; ++s)
                 if (ring_armed & (1u << s)) w.drain(full(s), (ring_parity >> s) & 1u);
         }
@@ -256,7 +270,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 if (item < 0) break;
                 const Item it = decode(item);
                 if (it.nkv_max == 0) continue;
-                if (!w.wait(qfull, n_q & 1u, kDevErrMmaFull)) break;
+                const int qb = (int)(n_q % Cfg::QBUF);      // this item's Q set (as the producer's)
+                if (!w.wait(qfull(qb), (n_q / Cfg::QBUF) & 1u, kDevErrMmaFull)) break;
                 ++n_q;
                 tcgen05_fence_after();
                 // PV_q(t) = P_q(t) V_t accumulated into O_q; V_t sits in the ring slot `s` the
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         if (j < it.nkv[q]) {
                             // S_q(j) = Q_q K_j^T, over P_q(j-1) (read by the PV just issued, or by
                             // the previous item's last PV_q: one thread's products complete in order)
-                            const uint32_t q_s = sb + Cfg::OFF_Q + q * Cfg::Q_BYTES;
+                            const uint32_t q_s = sb + Cfg::OFF_Q + (qb * NQ + q) * Cfg::Q_BYTES;
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
                                 const uint32_t off = (k >> 2) * Cfg::CHUNK_BYTES + (k & 3) * 32;
@@ -305,7 +320,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     }
                     if (!ok) break;
                     // every Q K^T product of the item is issued: Q may be replaced once they finish
-                    if (j == it.nkv_max - 1) mma_commit(qfree);
+                    if (j == it.nkv_max - 1) mma_commit(qfree(qb));
                     mma_commit(empty(s));
                 }
                 if (!ok) break;
