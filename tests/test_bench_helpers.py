@@ -72,6 +72,12 @@ def test_per_config_entry_fields():
     assert abs(e["median5_TFLOP/s"] - w.flops / 0.09e-3 / 1e12) < 1e-9
     assert abs(e["GB/s"] - w.bytes / 0.08e-3 / 1e9) < 1e-6
     assert e["roofline"]["bound"] == "hbm"
+    assert "l2_warm" not in e                       # timed back to back already
+    w1 = WORKLOADS["square1024"]                      # flushed: the warm figure rides along
+    rec1 = dict(rec, warm_ms=0.01)
+    e1 = bench.per_config_entry(w1, rec1, 0, "gsr_tiled_kernel", peaks, "measured", 1)
+    assert abs(e1["l2_warm"]["TFLOP/s"] - w1.flops / 0.01e-3 / 1e12) < 1e-9
+    assert "no flush" in e1["l2_warm"]["how"]
 
 
 def test_host_cpu_model_is_a_string():
