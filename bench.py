@@ -507,7 +507,7 @@ def run_gsr(args, w):
     kernel = KERNEL_NAMES[path]
     peaks, peaks_src = measured_peaks()
 
-    sampler = ClockSampler(gpu_uuid(), interval_ms=20).start() if rank == 0 else None
+    sampler = ClockSampler(gpu_uuid(), interval_ms=5).start() if rank == 0 else None
     rec, (A, B, dA, dB, dC, flush, step) = time_gemm(gsr, w, args, dev, stream, world, args.epilogue)
     t_wall0, t_wall1 = rec["wall"]
     inputs_bytes = (w.M * w.K + w.K * w.N) * 2
@@ -670,7 +670,7 @@ def run_attention(args, w):
         torch.cuda.synchronize()
         return sum(a.elapsed_time(b) for a, b in ev) / args.steps
 
-    sampler = ClockSampler(gpu_uuid()).start() if rank == 0 else None
+    sampler = ClockSampler(gpu_uuid(), interval_ms=5).start() if rank == 0 else None
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
