@@ -329,6 +329,33 @@ def test_streams_do_not_share_workspace():
         check(c.cpu(), ref, z, "stream")
 
 
+def test_every_gemm_kernel_on_two_streams_at_once():
+    # CTA-pair, one-CTA and small-M launches queued alternately on two streams, three rounds:
+    # whatever overlaps on the GPU, each result must match the oracle
+    dev = torch.device("cuda", 0)
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    shapes = [(2048, 4096, 512), (1000, 1024, 512), (16, 4096, 2048), (2304, 2560, 264)]
+    cases = []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B = make_inputs(M, N, K, seed=40 + i)
+        cases.append((A, B, A.to(dev), B.to(dev),
+                      torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)))
+    assert [gsr.select_path(M, N, K) for M, N, K in shapes] == [gsr.KERNEL_PAIR, gsr.KERNEL_TILED,
+                                                               gsr.KERNEL_SKINNY, gsr.KERNEL_PAIR]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for i, (_, _, dA, dB, dC) in enumerate(cases):
+            s = streams[i % 2]
+            with torch.cuda.stream(s):
+                gsr.gemm_scale_relu(dA, dB, dC, 0.5, stream=s)
+    for s in streams:
+        assert gsr.device_status(s)[0] == gsr.Status.OK
+    for A, B, _, _, dC in cases:
+        rows = sample_rows(A.shape[0])
+        ref, z = oracle.gemm_scale_relu(A, B, 0.5, rows=rows, return_pre=True)
+        check(dC.cpu()[rows], ref, z, "two streams %dx%dx%d" % (A.shape[0], B.shape[1], A.shape[1]))
+
+
 def test_host_entry_point_round_trip():
     M, N, K = 256, 384, 512
     A, B = make_inputs(M, N, K, seed=13)
