@@ -28,13 +28,21 @@
 namespace gsr {
 namespace {
 
-template <int BN_, int STAGES_>
+// BK = 64 is one TMA box of K (128 bytes); a stage holds KSUB such sub-blocks.  With the copies
+// taken out, the MMA issuer's loop took ~570 cycles per stage of 4 MMAs whatever N was (64, 128
+// or 256) and ~790 per stage of 8: at N = 64 or 128 (128 or 256 cycles of tensor work per
+// sub-block) one sub-block per stage leaves the tensor pipe idle most of the time, so those tiles
+// take two sub-blocks per stage (8 MMAs per wait and commit).  At N = 256 one sub-block is 512
+// cycles of tensor work, and two would leave room for only two stages (10 % slower).
+template <int BN_, int STAGES_, int KSUB_>
 struct TiledCfg {
-    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
+    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KSUB = KSUB_;
     static constexpr int NUM_THREADS = 192;                  // 6 warps
-    static constexpr int A_STAGE_BYTES = BM * BK * 2;        // 16 KB
+    static constexpr int A_SUB_BYTES = BM * BK * 2;          // 16 KB: one 64-wide K sub-block
     static constexpr int B_CHUNK_BYTES = BK * 64 * 2;        // one 64-column TMA box: 8 KB
-    static constexpr int B_STAGE_BYTES = BK * BN * 2;
+    static constexpr int B_SUB_BYTES = BK * BN * 2;
+    static constexpr int A_STAGE_BYTES = KSUB * A_SUB_BYTES;
+    static constexpr int B_STAGE_BYTES = KSUB * B_SUB_BYTES;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int C_CHUNK_COLS = 64;
     static constexpr int C_BUF_BYTES = BM * C_CHUNK_COLS * 2;  // 16 KB
@@ -113,10 +121,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             uint32_t armed_mask = 0, armed_parity = 0;   // last phase each stage was filled in
             bool drop_first = (p.test_flags & kTestDropFirstLoad) && blockIdx.x == 0;
             bool ok = true;
+            const int n_stages = (p.num_k_blocks + Cfg::KSUB - 1) / Cfg::KSUB;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 int mb, nb;
                 raster_tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = 0; kb < n_stages; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kDevErrProducerEmpty)) {
                         ok = false;
                         break;
@@ -126,12 +135,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     } else {
                         const uint32_t fb = full_bar(stage);
                         mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                        tma_load_2d(sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES, &tmA, fb,
-                                    kb * Cfg::BK, mb * Cfg::BM);
 #pragma unroll
-                        for (int j = 0; j < Cfg::BN / 64; ++j)
-                            tma_load_2d(sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES + j * Cfg::B_CHUNK_BYTES,
-                                        &tmB, fb, nb * Cfg::BN + j * 64, kb * Cfg::BK);
+                        for (int h = 0; h < Cfg::KSUB; ++h) {
+                            // sub-block h: K columns [(KSUB kb + h) 64, +64); past K, TMA fills
+                            // zeros (and still counts the whole box), which add nothing
+                            const int k0 = (kb * Cfg::KSUB + h) * Cfg::BK;
+                            tma_load_2d(sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES + h * Cfg::A_SUB_BYTES, &tmA,
+                                        fb, k0, mb * Cfg::BM);
+#pragma unroll
+                            for (int j = 0; j < Cfg::BN / 64; ++j)
+                                tma_load_2d(sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES + h * Cfg::B_SUB_BYTES +
+                                                j * Cfg::B_CHUNK_BYTES,
+                                            &tmB, fb, nb * Cfg::BN + j * 64, k0);
+                        }
                         armed_mask |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -149,25 +165,32 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true;
+            // Descriptors of stage 0, advanced by adding (byte offset >> 4) to their start-address
+            // field (bits 0-13): every operand lies below 232448 bytes, so the field cannot carry.
+            // Building each from scratch cost ~10 cycles per MMA in the issuing thread.
+            // A: K-major, 16 elements (32 bytes) per MMA inside the 128-byte swizzle row.
+            // B: MN-major, 16 K rows (2048 bytes) per MMA; 64-column chunks 8 KB apart.
+            const uint64_t a_desc0 = smem_desc_sw128(sb + Cfg::OFF_A, 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(sb + Cfg::OFF_B, Cfg::B_CHUNK_BYTES, 1024);
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
                 const uint32_t acc = it & 1u, acc_parity = (it >> 1) & 1u;
                 if (!w.wait(tempty_bar(acc), acc_parity ^ 1u, kDevErrMmaAccEmpty)) break;
                 tcgen05_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::BN;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                const int n_stages = (p.num_k_blocks + Cfg::KSUB - 1) / Cfg::KSUB;
+                for (int kb = 0; kb < n_stages; ++kb) {
                     if (!w.wait(full_bar(stage), phase, kDevErrMmaFull)) {
                         ok = false;
                         break;
                     }
                     tcgen05_fence_after();
-                    const uint32_t a0 = sb + Cfg::OFF_A + stage * Cfg::A_STAGE_BYTES;
-                    const uint32_t b0 = sb + Cfg::OFF_B + stage * Cfg::B_STAGE_BYTES;
+                    const uint64_t ad_s = a_desc0 + (uint64_t)((stage * Cfg::A_STAGE_BYTES) >> 4);
+                    const uint64_t bd_s = b_desc0 + (uint64_t)((stage * Cfg::B_STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < Cfg::BK / 16; ++k) {
-                        // A: K-major, advance 16 elements = 32 bytes inside the swizzle row.
-                        const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
-                        // B: MN-major, advance 16 K rows = 2048 bytes; 64-column chunks 8 KB apart.
-                        const uint64_t bd = smem_desc_sw128(b0 + k * 2048, Cfg::B_CHUNK_BYTES, 1024);
+                    for (int k = 0; k < Cfg::KSUB * Cfg::BK / 16; ++k) {
+                        const uint32_t hs = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+                        const uint64_t ad = ad_s + (uint64_t)((hs * Cfg::A_SUB_BYTES + kk * 32) >> 4);
+                        const uint64_t bd = bd_s + (uint64_t)((hs * Cfg::B_SUB_BYTES + kk * 2048) >> 4);
                         mma_f16_ss(d_tmem, ad, bd, Cfg::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
@@ -238,9 +261,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     }
 }
 
-using Cfg256 = TiledCfg<256, 4>;
-using Cfg128 = TiledCfg<128, 6>;
-using Cfg64 = TiledCfg<64, 8>;
+using Cfg256 = TiledCfg<256, 4, 1>;
+using Cfg128 = TiledCfg<128, 3, 2>;
+using Cfg64 = TiledCfg<64, 4, 2>;
 
 template <class Cfg>
 cudaError_t launch_cfg(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,

@@ -290,15 +290,23 @@ int pair_path(int64_t M, int64_t N, int num_sms) {
 // wave the narrow tiles win (64 tiles: 1024 x 2048 x 1024 14.0 against 12.6, 512 x 4096 x 2048
 // 18.7 against 17.4; 32 tiles: 1024^3 13.9 against 12.6).  Counting waves, not tiles, also
 // keeps N = 128 on 128-wide tiles, where a 256-wide one is half empty (16384 x 128 x 4096:
-// 27.6 against 31.1 us).  64-wide tiles (path override 7) are a sweep candidate only: on 1024^3
-// they took the same time as 128-wide ones and lost on every larger shape measured.
+// 27.6 against 31.1 us).
 constexpr double kWideTileCost = 1.45;
+
+// 128 x 64 tiles: a wave of them costs kNarrowTileCost waves of 128 x 128 tiles (a stage of
+// 48 KB instead of 64 KB per SM, and half the epilogue), so they are taken when they still fit
+// in one wave.  L2 flushed, median of 5 x 100 calls: 1024^3 10.7 us against 11.3, 1000 x 1000 x
+// 200 9.1 against 10.1, 1024 x 1024 x 4096, 512 x 2048 x 4096 and 768 x 1536 x 2048 within 1 %;
+// at two waves they lose (1024 x 2048 x 1024: 14.7 against 12.4).
+constexpr double kNarrowTileCost = 0.9;
 
 int tiled_width(long long mb, int64_t N, int num_sms) {
     const long long sms = num_sms > 0 ? num_sms : 1;
-    const long long t256 = mb * ((N + 255) / 256), t128 = mb * ((N + 127) / 128);
+    const long long t256 = mb * ((N + 255) / 256), t128 = mb * ((N + 127) / 128), t64 = mb * ((N + 63) / 64);
     const double w256 = kWideTileCost * (double)((t256 + sms - 1) / sms);
     const double w128 = (double)((t128 + sms - 1) / sms);
+    const double w64 = kNarrowTileCost * (double)((t64 + sms - 1) / sms);
+    if (w64 < w128 && w64 < w256) return 64;
     return w256 < w128 ? 256 : 128;
 }
 

@@ -135,9 +135,12 @@ CHOICE_SHAPES = [(2048, 2048, 2048), (2304, 2304, 2048), (1792, 2560, 2048), (20
                  (4096, 1024, 4096), (4096, 1280, 4096), (16384, 128, 4096), (16384, 384, 4096),
                  (16384, 640, 4096), (16384, 1152, 4096), (3072, 3072, 1024), (6144, 6144, 2048),
                  (1536, 2048, 2048), (1024, 2048, 1024), (1280, 2048, 2048), (2000, 3000, 1000),
-                 (1024, 1024, 1024), (8192, 384, 4096), (12288, 192, 4096)]
+                 (1024, 1024, 1024), (8192, 384, 4096), (12288, 192, 4096), (1024, 1024, 4096),
+                 (1000, 1000, 200), (768, 1536, 2048), (1024, 1536, 1024), (512, 2048, 4096),
+                 (1152, 2048, 1024)]
 CHOICE_KERNELS = {"auto": gsr.PATH_AUTO, "tiled_128x256": gsr.PATH_TILED_256,
-                  "tiled_128x128": gsr.PATH_TILED_128, "pair_256x256": gsr.PATH_PAIR,
+                  "tiled_128x128": gsr.PATH_TILED_128, "tiled_128x64": gsr.PATH_TILED_64,
+                  "pair_256x256": gsr.PATH_PAIR,
                   "pair_256x128": gsr.PATH_PAIR_128}
 FLUSH_BELOW = 100 << 20   # operands smaller than this would stay in L2 between calls
 
