@@ -153,17 +153,21 @@ __device__ __forceinline__ uint4 epilogue_8(const uint32_t* src, float alpha, in
 // at j ^ (r & 7): conflict-free), and hand the buffer to one TMA store of the box at (col0, m0),
 // which clips whatever lies outside C.  Named barrier 1 spans the 128 epilogue threads; `et`
 // is the thread's index among them.  `pol`, when `hinted`, is the L2 policy of the written lines.
+// KIND >= 0 fixes the epilogue kind at compile time (p.epi must equal it), so that the eight
+// groups of values carry no branch on it; KIND = -1 reads p.epi.
+template <int KIND = -1>
 __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
                                                      uint8_t* buf, uint32_t buf_saddr, int row, int et,
                                                      const TiledParams& p, int col0, int m0,
                                                      const CUtensorMap* tmC, bool hinted, uint64_t pol) {
+    const int epi = KIND >= 0 ? KIND : p.epi;
     if (et == 0) bulk_wait_group_read<1>();   // the store from this buffer is done reading it
     named_bar_sync(1, 128);
     uint8_t* crow = buf + row * 128;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint32_t* src = (j < 4) ? (r0 + 8 * j) : (r1 + 8 * (j - 4));
-        const uint4 v = epilogue_8(src, p.alpha, p.epi, p.bias, col0 + 8 * j, p.N);
+        const uint4 v = epilogue_8(src, p.alpha, epi, p.bias, col0 + 8 * j, p.N);
         *reinterpret_cast<uint4*>(crow + ((j ^ (row & 7)) << 4)) = v;
     }
     fence_proxy_async_smem();

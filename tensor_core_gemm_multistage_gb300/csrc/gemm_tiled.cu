@@ -243,9 +243,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     mbar_arrive(tempty_bar(acc));   // MMA may now overwrite this accumulator
                 }
                 const uint32_t buf = cidx & 1u;
-                epilogue_store_chunk(r0, r1, smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES,
-                                     sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES, row, et, p, n0 + c * 64, m0,
-                                     &tmC, false, 0);
+                uint8_t* const cbuf = smem + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES;
+                const uint32_t cbuf_s = sb + Cfg::OFF_C + buf * Cfg::C_BUF_BYTES;
+                // one copy of the chunk's code per epilogue kind (the kind is the same for every
+                // chunk of the launch): the values of a chunk then convert without a branch
+                if (p.epi == kEpiScaleRelu)
+                    epilogue_store_chunk<kEpiScaleRelu>(r0, r1, cbuf, cbuf_s, row, et, p, n0 + c * 64, m0, &tmC, false, 0);
+                else if (p.epi == kEpiScale)
+                    epilogue_store_chunk<kEpiScale>(r0, r1, cbuf, cbuf_s, row, et, p, n0 + c * 64, m0, &tmC, false, 0);
+                else
+                    epilogue_store_chunk<kEpiBiasGelu>(r0, r1, cbuf, cbuf_s, row, et, p, n0 + c * 64, m0, &tmC, false, 0);
                 ++cidx;
             }
         }
