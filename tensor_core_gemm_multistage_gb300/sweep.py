@@ -22,9 +22,9 @@ kernel the library picks on its own.
 
     python -m tensor_core_gemm_multistage_gb300.sweep --check-choice
 
-times the library's own choice against each of the four main kernels (default knobs) on
+times the library's own choice against each of the five main kernels (default knobs) on
 shapes around the boundaries of that choice (pair against one-CTA tiles, 256- against
-128-wide pair tiles, 256- against 128-wide one-CTA tiles), one JSON line per shape with the
+128-wide pair tiles, 256- against 128- against 64-wide one-CTA tiles), one JSON line per shape with the
 ratio of the choice's time to the fastest kernel's.  Timing: CUDA events around back-to-back calls after
 warm-up, as the tutorial's benchmark_op does; every configuration is timed in several
 rounds of shuffled order and the median is kept.  A development tool; nothing here changes the
