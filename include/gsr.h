@@ -238,8 +238,9 @@ gsr_status gsr_device_status(struct CUstream_st* stream, int* code);
 gsr_status gsr_release_stream(struct CUstream_st* stream);
 
 /* Kernel the library would run for these sizes on the current device: 0 = tiled
- * (one CTA per 128-row tile, 128 x 256 or 128 x 128 tiles, whichever needs fewer
- * waves with a wave of the wider ones counted as 1.45), 1 = small-M (M <= 64),
+ * (one CTA per 128-row tile, 128 x 256, 128 x 128 or 128 x 64 tiles, whichever
+ * needs fewer waves with a wave of 256-wide tiles counted as 1.45 and one of 64-wide
+ * tiles as 0.9 of a wave of 128-wide ones), 1 = small-M (M <= 64),
  * 2 = tiled on CTA pairs with 256 x 256 tiles (chosen when there is at least one
  * full wave of such tiles), 3 = tiled on CTA pairs with 256 x 128 tiles (instead
  * of 2 where a wave of them, counted as 0.68 of a wide wave, finishes the work at

@@ -7,8 +7,8 @@
 // Epilogue: scale and ReLU applied on chip before the single write-back).
 //
 // The GB300 design keeps those steps and changes how each one is carried out:
-//  * tile 128 x BN x 64 (BN = 256, 128 or 64) instead of 64 x 64 x 32, because one tcgen05
-//    MMA covers 128 x BN x 16 (the 64-wide tile is a tuning-sweep candidate);
+//  * tile 128 x BN (BN = 256, 128 or 64) with K in 64-wide sub-blocks, one or two per
+//    pipeline stage, instead of 64 x 64 x 32, because one tcgen05 MMA covers 128 x BN x 16;
 //  * a persistent grid (one CTA per SM) walks the tiles in grouped-M order so
 //    neighbouring CTAs share A and B panels in L2;
 //  * warp roles: warp 0 issues TMA loads into a STAGES-deep shared-memory ring
