@@ -126,3 +126,29 @@ def test_bias_gelu_validation_on_device():
         == gsr.Status.ERR_ALIGNMENT
     assert p(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), dC.data_ptr(), 64, 64, 64) \
         == gsr.Status.ERR_ALIAS
+
+
+@pytest.mark.parametrize("path", [gsr.PATH_PAIR, gsr.PATH_PAIR_128])
+def test_pair_epilogues_beyond_two_waves(path):
+    # The pair kernel has two copies: launches of at most two waves of work units (every shape
+    # above) run the one whose epilogue loop is compiled per kind, longer launches the one that
+    # reads the kind at run time.  This shape gives 190 units of 256 x 256 (171 tiles, the last
+    # wave in halves) or 342 of 256 x 128 on 76 pairs: the second copy, every kind, checked whole.
+    M, N, K = 2304, 4864, 136
+    A, B = make_inputs(M, N, K, seed=11, b_std_inv_sqrt_k=True)
+    C = run(oracle.EPI_SCALE, A, B, -0.75, path=path)
+    check(C, oracle.gemm_epilogue(A, B, -0.75, oracle.EPI_SCALE), "scale path=%d" % path)
+    bias = make_bias(N, seed=12)
+    C = run(oracle.EPI_BIAS_GELU, A, B, bias=bias, path=path)
+    check(C, oracle.gemm_epilogue(A, B, kind=oracle.EPI_BIAS_GELU, bias=bias), "bias_gelu path=%d" % path)
+    dev = torch.device("cuda", 0)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    gsr.set_path_override(path)
+    try:
+        gsr.gemm_scale_relu(dA, dB, dC, 0.5)
+        status, code = gsr.device_status()
+    finally:
+        gsr.set_path_override(gsr.PATH_AUTO)
+    assert status == gsr.Status.OK, hex(code)
+    check(dC.cpu().numpy(), oracle.gemm_scale_relu(A, B, 0.5), "scale_relu path=%d" % path)
