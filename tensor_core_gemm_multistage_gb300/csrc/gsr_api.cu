@@ -310,7 +310,17 @@ int tiled_width(long long mb, int64_t N, int num_sms) {
     return w256 < w128 ? 256 : 128;
 }
 
-int choose_path(int64_t M, int64_t N, int num_sms) {
+// Below a full wave of 256 x 256 pair tiles the one-CTA kernel is taken, except where it would
+// run 128 x 256 tiles (two SMs per 256 x 256 of C, as a pair tile) over a long K.  Per 64-wide K
+// sub-block a pair's SM spends ~500 cycles (N = 256 MMAs), a single tile's ~660 (its 48 KB
+// stage is copy-bound), which from K of about 6000 on repays the pair's larger cost per launch
+// (its first cluster barrier and paired TMEM release, and a slower start).  L2 flushed where A
+// and B fit in it, median of 5 rounds: K = 4096, single tiles 1-3 % faster (256 x 16384,
+// 4096 x 1024, 8192 x 384); K = 8192, pairs 1.5-4.7 % faster (256 x 16384, 2048 x 2048,
+// 1024 x 4096, 4096 x 1024, 512 x 8192); K = 16384, pairs 3.3-6.5 % (256 x 16384, 2048 x 2048).
+constexpr int64_t kPairMinK = 6144;
+
+int choose_path(int64_t M, int64_t N, int64_t K, int num_sms) {
     const int o = g_path_override.load(std::memory_order_relaxed);
     if (o == 1 || o == 3 || o == 4 || o == 7) return 0;
     if (o == 5) return 2;
@@ -318,7 +328,9 @@ int choose_path(int64_t M, int64_t N, int num_sms) {
     if (o == 2 && M <= kSkinnyMaxM) return 1;
     if (M <= kSkinnyMaxM) return 1;
     const long long pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    return pair_tiles >= num_sms / 2 ? pair_path(M, N, num_sms) : 0;
+    if (pair_tiles >= num_sms / 2) return pair_path(M, N, num_sms);
+    if (K >= kPairMinK && tiled_width((M + 127) / 128, N, num_sms) == 256) return pair_path(M, N, num_sms);
+    return 0;
 }
 
 constexpr int kDefaultSms = 152;   // for gsr_select_path before any device is touched
@@ -486,7 +498,7 @@ gsr_status gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N
         return e == cudaSuccess ? GSR_OK : cuda_fail(e);
     }
     if ((s = load_encoder()) != GSR_OK) return s;
-    const int path = choose_path(M, N, info.num_sms);
+    const int path = choose_path(M, N, K, info.num_sms);
     if (path == 1) return run_skinny(A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
     if (path == 2 || path == 3)
         return run_pair(path == 3 ? 128 : 256, A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info);
@@ -506,7 +518,7 @@ gsr_status gemm_block(const void* A, const void* B, void* C, int64_t M, int64_t 
     if ((s = load_encoder()) != GSR_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Epi ep{gsr::kEpiScaleRelu, nullptr};
-    const int path = choose_path(M, N, info.num_sms);
+    const int path = choose_path(M, N, K, info.num_sms);
     if (path == 1) return GSR_ERR_INVALID_ARG;
     if (path == 2 || path == 3)
         return run_pair(path == 3 ? 128 : 256, A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info,
@@ -912,7 +924,6 @@ gsr_status gsr_release_stream(CUstream_st* stream) {
 }
 
 int gsr_select_path(int64_t M, int64_t N, int64_t K) {
-    (void)K;
     int sms = kDefaultSms;
     int dev = 0;
     {
@@ -922,7 +933,7 @@ int gsr_select_path(int64_t M, int64_t N, int64_t K) {
             if (it != g_devices.end()) sms = it->second.num_sms;
         }
     }
-    return choose_path(M, N, sms);
+    return choose_path(M, N, K, sms);
 }
 
 void gsr_set_path_override(int path) { g_path_override.store(path, std::memory_order_relaxed); }

@@ -115,6 +115,14 @@ def test_path_selection_and_override():
         assert gsr.select_path(16384, 384, 4096) == gsr.KERNEL_PAIR
         assert gsr.select_path(16384, 640, 4096) == gsr.KERNEL_PAIR
         assert gsr.select_path(4096, 4096, 4096) == gsr.KERNEL_PAIR
+        # below a full wave of pair tiles: 128 x 256 single tiles up to K ~ 6000, pairs beyond
+        # (their faster K loop repays their larger cost per launch); 128 x 128 single tiles,
+        # which use twice the SMs, stay at any K
+        assert gsr.select_path(256, 16384, 4096) == gsr.KERNEL_TILED
+        assert gsr.select_path(256, 16384, 8192) == gsr.KERNEL_PAIR
+        assert gsr.select_path(2048, 2048, 2048) == gsr.KERNEL_TILED
+        assert gsr.select_path(2048, 2048, 16384) == gsr.KERNEL_PAIR
+        assert gsr.select_path(1024, 2048, 16384) == gsr.KERNEL_TILED
         gsr.set_path_override(gsr.PATH_TILED)
         assert gsr.select_path(16, 16384, 16384) == 0
         assert gsr.select_path(8192, 8192, 8192) == 0
