@@ -120,6 +120,8 @@ def test_path_selection_and_override():
         # which use twice the SMs, stay at any K
         assert gsr.select_path(256, 16384, 4096) == gsr.KERNEL_TILED
         assert gsr.select_path(256, 16384, 8192) == gsr.KERNEL_PAIR
+        assert gsr.select_path(256, 16384, 6136) == gsr.KERNEL_TILED
+        assert gsr.select_path(256, 16384, 6144) == gsr.KERNEL_PAIR
         assert gsr.select_path(2048, 2048, 2048) == gsr.KERNEL_TILED
         assert gsr.select_path(2048, 2048, 16384) == gsr.KERNEL_PAIR
         assert gsr.select_path(1024, 2048, 16384) == gsr.KERNEL_TILED

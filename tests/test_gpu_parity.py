@@ -511,3 +511,14 @@ def test_a_long_k(path):
     C = run_gpu(A, B, 1.0, path)
     ref, z = oracle.gemm_scale_relu(A, B, 1.0, return_pre=True)
     check(C, ref, z, "K=2^17-8 path %d" % path)
+
+
+@pytest.mark.parametrize("K", [6136, 6144])
+def test_pairs_below_a_wave_from_a_long_k(K):
+    # 256 x 16384: 64 pair tiles, fewer than the 76 pairs of a wave.  Up to K = 6143 the library
+    # takes 128 x 256 one-CTA tiles, from 6144 on CTA pairs (their faster K loop repays their
+    # cost per launch); both sides of that boundary, checked on rows of both 128-row halves of
+    # the pair tile and the last row
+    M, N = 256, 16384
+    assert gsr.select_path(M, N, K) == (gsr.KERNEL_TILED if K < 6144 else gsr.KERNEL_PAIR)
+    parity(M, N, K, 1.0, seed=K, b_scaled=True, rows=[0, 1, 63, 127, 128, 129, 200, 255])
