@@ -192,8 +192,7 @@ gsr_status gemm_scale_relu_host(const void* hA, const void* hB, void* hC, void* 
  * default lazy module loading, that is when the driver places the array and the
  * kernels' code on the device: an allocation by the driver, which can also
  * synchronise.  A caller with a fixed memory plan should therefore make one call
- * on each device during start-up, and before any stream capture.  Later calls
- * place nothing.
+ * on each device during start-up.  Later calls place nothing.
  *
  * Every call shares the array and it keeps the last call's contents; each call
  * clears the parts that must start at zero, on `stream`, before its kernel.
