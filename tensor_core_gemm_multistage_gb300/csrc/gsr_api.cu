@@ -261,7 +261,8 @@ int pair_full_tiles(int num_tiles, int clusters, int bn) {
 }
 
 // 0: tiled, one CTA per 128 x BN tile; 1: small-M; 2: tiled on CTA pairs (256 x 256 tiles),
-// taken when there are at least as many pair tiles as half the SMs (one full wave of pairs).
+// taken when there are at least as many pair tiles as half the SMs (one full wave of pairs), or
+// below that for a long K where the one-CTA kernel would take 128 x 256 tiles (choose_path).
 // Pair tiles 256 wide (with a last wave of half tiles where that helps), or 128 wide where
 // that is estimated to be faster: time ~ waves x tile cost, a wave of 256 x 128 tiles or half
 // units costing kHalfTileCost of a wave of 256 x 256 tiles (half the MMAs plus the fixed
@@ -285,12 +286,11 @@ int pair_path(int64_t M, int64_t N, int num_sms) {
 // Tile width of the one-CTA-per-tile kernel: whichever finishes first when a wave of
 // 128 x 256 tiles costs kWideTileCost waves of 128 x 128 tiles (an N = 256 MMA does twice the
 // work of an N = 128 one in ~1.45x the time, and its tile stages 1.5x the bytes per k-block).
-// L2 flushed, mean of 200 calls: 2048^3 with 128 tiles of 128 x 256 19.2 us against 26.9 with
-// 256 of 128 x 128, 1536 x 2048 x 2048 with 96 tiles 19.2 against 25.7, while below half a
-// wave the narrow tiles win (64 tiles: 1024 x 2048 x 1024 14.0 against 12.6, 512 x 4096 x 2048
-// 18.7 against 17.4; 32 tiles: 1024^3 13.9 against 12.6).  Counting waves, not tiles, also
-// keeps N = 128 on 128-wide tiles, where a 256-wide one is half empty (16384 x 128 x 4096:
-// 27.6 against 31.1 us).
+// L2 flushed, median of 5 x 100 calls, 128-wide tiles at 8 MMAs per stage: 2048^3 with 128
+// tiles of 128 x 256 18.8 us against 20.9 with 256 of 128 x 128, 1536 x 2048 x 2048 with 96
+// tiles 17.6 against 20.7, while below half a wave the narrow tiles win (64 tiles: 1024 x 2048
+// x 1024 12.6 against 11.2).  Counting waves, not tiles, also keeps N = 128 on 128-wide tiles,
+// where a 256-wide one is half empty (16384 x 128 x 4096: 27.1 against 31.1 us).
 constexpr double kWideTileCost = 1.45;
 
 // 128 x 64 tiles: a wave of them costs kNarrowTileCost waves of 128 x 128 tiles (a stage of
