@@ -251,7 +251,9 @@ int gsr_select_path(int64_t M, int64_t N, int64_t K);
 
 /* Forces a path for later calls (process-wide): 0 = automatic (default),
  * 1 = tiled with automatic tile width, 2 = small-M (only honoured when
- * M <= 64), 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles,
+ * M <= 256: 65 to 256 rows run with an MMA N of 128 or 256, which the automatic
+ * choice does not take; the host-buffer entry point's blocks ignore it),
+ * 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles,
  * 5 = tiled on CTA pairs with 256 x 256 tiles, 6 = tiled on CTA pairs with
  * 256 x 128 tiles, 7 = tiled with 128 x 64 tiles.
  * For tests and measurements. */

@@ -1,13 +1,14 @@
-// gemm_skinny.cu - small-M path of C = ReLU(alpha * A.B) on sm_103a (M <= 64).
+// gemm_skinny.cu - small-M path of C = ReLU(alpha * A.B) on sm_103a (M <= 64; up to 256 when forced).
 //
 // Same operator as the tiled path ("Tutorial14: 使用TileLang语言编写attention算子",
 // section 3 formula; section 2 kernel: float accumulator, scale, max with 0, fp16 out).
 // When M is a handful of rows the work is streaming B (K x N) from HBM once; a 128-row
 // M tile would leave most of each MMA empty and only ceil(N/BN) CTAs busy.  So:
 //  * swap A and B: the MMA computes C^T (N x M) = B^T (N x K) . A^T (K x M), with
-//    128 columns of C per tile as the MMA's M and M (rounded up to MP = 16/32/64) as
-//    its N.  B^T is read straight from row-major B as an MN-major operand and A^T from
-//    row-major A as a K-major operand: nothing is transposed in memory;
+//    128 columns of C per tile as the MMA's M and M (rounded up to MP = 16/32/64, or
+//    128/256 when the path is forced for 65 to 256 rows) as its N.  B^T is read straight
+//    from row-major B as an MN-major operand and A^T from row-major A as a K-major
+//    operand: nothing is transposed in memory;
 //  * split K into S equal slabs per tile (S = #SMs / #tiles, at least 1): work item w =
 //    (slab w / T, tile w % T) for T tiles, so the CTAs running at one time work on the
 //    same slab and walk through the same rows of B in step, as one streaming pass (DRAM
@@ -36,7 +37,7 @@ struct SkinnyCfg {
     static constexpr int BT_STAGE_BYTES = BK * TN * 2;   // 16 KB
     static constexpr int AT_STAGE_BYTES = MP * BK * 2;   // MP rows of A, 128 bytes each
     static constexpr int STAGE_BYTES = BT_STAGE_BYTES + AT_STAGE_BYTES;
-    static constexpr int TMEM_COLS = (2 * MP <= 32) ? 32 : (2 * MP <= 64 ? 64 : 128);
+    static constexpr int TMEM_COLS = (2 * MP <= 32) ? 32 : (2 * MP <= 64 ? 64 : (2 * MP <= 128 ? 128 : (2 * MP <= 256 ? 256 : 512)));
     static constexpr int OFF_BT = 0;
     static constexpr int OFF_AT = OFF_BT + STAGES * BT_STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_AT + STAGES * AT_STAGE_BYTES;
@@ -45,7 +46,8 @@ struct SkinnyCfg {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_f16_f32(TN, MP, /*a_mn=*/true, /*b_mn=*/false);
 
-    static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "MP must be 16, 32, 48 or 64");
+    static_assert(MP % 16 == 0 && MP >= 16 && (MP <= 64 || MP == 128 || MP == 256),
+                  "MP must be 16, 32, 48, 64, 128 or 256");
     static_assert(AT_STAGE_BYTES % 1024 == 0, "A^T stage must keep 1024-byte alignment");
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-CTA shared-memory limit");
 };
@@ -210,63 +212,136 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             }
             tcgen05_fence_after();
 
-            float v[MP];
-            {
-                const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * MP;
+            if constexpr (MP <= 64) {
+                float v[MP];
+                {
+                    const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * MP;
 #pragma unroll
-                for (int c = 0; c < MP / 16; ++c) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(t_row + c * 16, r);
-                    tmem_ld_wait(r);
+                    for (int c = 0; c < MP / 16; ++c) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(t_row + c * 16, r);
+                        tmem_ld_wait(r);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
+                        for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
+                    }
                 }
-            }
-            tcgen05_fence_before();
-            mbar_arrive(tempty_bar(acc));
+                tcgen05_fence_before();
+                mbar_arrive(tempty_bar(acc));
 
-            const int n = tile * Cfg::TN + nl;
-            bool store = true;
-            if (S > 1) {
-                // One slab of a tile: publish the partial, take a ticket.
-                float* mine = p.partials + ((size_t)tile * S + slab) * (MP * Cfg::TN);
+                const int n = tile * Cfg::TN + nl;
+                bool store = true;
+                if (S > 1) {
+                    // One slab of a tile: publish the partial, take a ticket.
+                    float* mine = p.partials + ((size_t)tile * S + slab) * (MP * Cfg::TN);
 #pragma unroll
-                for (int m = 0; m < MP; ++m) mine[m * Cfg::TN + nl] = v[m];
-                __threadfence();
-                named_bar_sync(1, 128);
-                if (et == 0) {
-                    const int old = atomicAdd(p.tickets + tile, 1);
-                    *s_last = (old + 1 == S) ? 1 : 0;
-                }
-                named_bar_sync(1, 128);
-                store = (*s_last != 0);
-                if (store) {
-                    // Last slab to finish: sum the tile's partials in slab order.
+                    for (int m = 0; m < MP; ++m) mine[m * Cfg::TN + nl] = v[m];
                     __threadfence();
-                    float sum[MP];
+                    named_bar_sync(1, 128);
+                    if (et == 0) {
+                        const int old = atomicAdd(p.tickets + tile, 1);
+                        *s_last = (old + 1 == S) ? 1 : 0;
+                    }
+                    named_bar_sync(1, 128);
+                    store = (*s_last != 0);
+                    if (store) {
+                        // Last slab to finish: sum the tile's partials in slab order.
+                        __threadfence();
+                        float sum[MP];
 #pragma unroll
-                    for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
-                    for (int q = 0; q < S; ++q) {
-                        if (q == slab) {
+                        for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
+                        for (int q = 0; q < S; ++q) {
+                            if (q == slab) {
 #pragma unroll
-                            for (int m = 0; m < MP; ++m) sum[m] += v[m];
-                        } else {
-                            const float* src = p.partials + ((size_t)tile * S + q) * (MP * Cfg::TN);
+                                for (int m = 0; m < MP; ++m) sum[m] += v[m];
+                            } else {
+                                const float* src = p.partials + ((size_t)tile * S + q) * (MP * Cfg::TN);
 #pragma unroll
-                            for (int m = 0; m < MP; ++m) sum[m] += __ldcg(src + m * Cfg::TN + nl);
+                                for (int m = 0; m < MP; ++m) sum[m] += __ldcg(src + m * Cfg::TN + nl);
+                            }
+                        }
+#pragma unroll
+                        for (int m = 0; m < MP; ++m) v[m] = sum[m];
+                        if (et == 0) p.tickets[tile] = 0;   // ready for the next launch
+                    }
+                }
+                if (store && n < p.N) {
+                    const float b = (p.epi == kEpiBiasGelu) ? __half2float(p.bias[n]) : 0.0f;
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        if (m < p.M)
+                            p.C[(size_t)m * p.N + n] = __float2half_rn(epilogue_value(v[m], p.alpha, b, p.epi));
+                }
+            } else {
+                // MMA N of 128 or 256: a whole row of the accumulator would not fit in registers,
+                // so every step walks it in chunks of 32 columns (rows m of C), reading them from
+                // tensor memory again where it needs them, and gives the accumulator back only
+                // after the last read.
+                constexpr int CH = 32;
+                const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * MP;
+                const int n = tile * Cfg::TN + nl;
+                bool store = true;
+                if (S > 1) {
+                    // One slab of a tile: publish the partial, take a ticket.
+                    float* mine = p.partials + ((size_t)tile * S + slab) * (MP * Cfg::TN);
+                    for (int c = 0; c < MP / CH; ++c) {
+                        uint32_t r[CH];
+                        tmem_ld_32x32b_x32(t_row + c * CH, r);
+                        tmem_ld_wait(r);
+#pragma unroll
+                        for (int i = 0; i < CH; ++i) mine[(c * CH + i) * Cfg::TN + nl] = __uint_as_float(r[i]);
+                    }
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (et == 0) {
+                        const int old = atomicAdd(p.tickets + tile, 1);
+                        *s_last = (old + 1 == S) ? 1 : 0;
+                    }
+                    named_bar_sync(1, 128);
+                    store = (*s_last != 0);
+                    if (store) __threadfence();
+                }
+                if (store) {
+                    // (the last slab to finish sums the tile's partials in slab order, its own
+                    // from tensor memory, then applies the epilogue)
+                    const float b = (p.epi == kEpiBiasGelu && n < p.N) ? __half2float(p.bias[n]) : 0.0f;
+                    for (int c = 0; c < MP / CH; ++c) {
+                        uint32_t r[CH];
+                        tmem_ld_32x32b_x32(t_row + c * CH, r);
+                        tmem_ld_wait(r);
+                        float v[CH];
+#pragma unroll
+                        for (int i = 0; i < CH; ++i) v[i] = __uint_as_float(r[i]);
+                        if (S > 1) {
+                            float sum[CH];
+#pragma unroll
+                            for (int i = 0; i < CH; ++i) sum[i] = 0.0f;
+                            for (int q = 0; q < S; ++q) {
+                                if (q == slab) {
+#pragma unroll
+                                    for (int i = 0; i < CH; ++i) sum[i] += v[i];
+                                } else {
+                                    const float* src = p.partials + ((size_t)tile * S + q) * (MP * Cfg::TN);
+#pragma unroll
+                                    for (int i = 0; i < CH; ++i) sum[i] += __ldcg(src + (c * CH + i) * Cfg::TN + nl);
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < CH; ++i) v[i] = sum[i];
+                        }
+                        if (n < p.N) {
+#pragma unroll
+                            for (int i = 0; i < CH; ++i) {
+                                const int m = c * CH + i;
+                                if (m < p.M)
+                                    p.C[(size_t)m * p.N + n] =
+                                        __float2half_rn(epilogue_value(v[i], p.alpha, b, p.epi));
+                            }
                         }
                     }
-#pragma unroll
-                    for (int m = 0; m < MP; ++m) v[m] = sum[m];
-                    if (et == 0) p.tickets[tile] = 0;   // ready for the next launch
+                    if (S > 1 && et == 0) p.tickets[tile] = 0;   // ready for the next launch
                 }
-            }
-            if (store && n < p.N) {
-                const float b = (p.epi == kEpiBiasGelu) ? __half2float(p.bias[n]) : 0.0f;
-#pragma unroll
-                for (int m = 0; m < MP; ++m)
-                    if (m < p.M)
-                        p.C[(size_t)m * p.N + n] = __float2half_rn(epilogue_value(v[m], p.alpha, b, p.epi));
+                tcgen05_fence_before();
+                mbar_arrive(tempty_bar(acc));
             }
         }
     }
@@ -283,6 +358,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 using Sk16 = SkinnyCfg<16, 11>;
 using Sk32 = SkinnyCfg<32, 10>;
 using Sk64 = SkinnyCfg<64, 8>;
+using Sk128 = SkinnyCfg<128, 6>;
+using Sk256 = SkinnyCfg<256, 4>;
 
 template <class Cfg>
 cudaError_t launch_cfg(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
@@ -305,7 +382,9 @@ cudaError_t launch_cfg(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const S
 }  // namespace
 
 int skinny_smem_bytes(int mp) {
-    return mp <= 16 ? Sk16::SMEM_BYTES : (mp <= 32 ? Sk32::SMEM_BYTES : Sk64::SMEM_BYTES);
+    return mp <= 16 ? Sk16::SMEM_BYTES
+                    : (mp <= 32 ? Sk32::SMEM_BYTES
+                                : (mp <= 64 ? Sk64::SMEM_BYTES : (mp <= 128 ? Sk128::SMEM_BYTES : Sk256::SMEM_BYTES)));
 }
 
 cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
@@ -313,6 +392,8 @@ cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, cons
     if (mp == 16) return launch_cfg<Sk16>(tmBt, tmAt, p, stream);
     if (mp == 32) return launch_cfg<Sk32>(tmBt, tmAt, p, stream);
     if (mp == 64) return launch_cfg<Sk64>(tmBt, tmAt, p, stream);
+    if (mp == 128) return launch_cfg<Sk128>(tmBt, tmAt, p, stream);
+    if (mp == 256) return launch_cfg<Sk256>(tmBt, tmAt, p, stream);
     return cudaErrorInvalidValue;
 }
 

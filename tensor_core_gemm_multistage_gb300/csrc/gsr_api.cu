@@ -29,6 +29,8 @@ std::atomic<int> g_raster_group{0};   // 0: each kernel's default grouping
 std::atomic<int> g_split_k{0};        // 0: the small-M kernel's own slab count
 
 constexpr int kSkinnyMaxM = 64;
+// The small-M kernel also runs up to 256 rows (MMA N of 128 or 256) when forced.
+constexpr int kSkinnyMaxForcedM = 256;
 constexpr int kGroupM = 16;
 
 // Device words per (device, stream): [0] the error word of kernels on the stream, [1] and [2]
@@ -325,7 +327,7 @@ int choose_path(int64_t M, int64_t N, int64_t K, int num_sms) {
     if (o == 1 || o == 3 || o == 4 || o == 7) return 0;
     if (o == 5) return 2;
     if (o == 6) return 3;
-    if (o == 2 && M <= kSkinnyMaxM) return 1;
+    if (o == 2 && M <= kSkinnyMaxForcedM) return 1;
     if (M <= kSkinnyMaxM) return 1;
     const long long pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     if (pair_tiles >= num_sms / 2) return pair_path(M, N, num_sms);
@@ -440,7 +442,7 @@ gsr_status run_pair(int bn, const void* A, const void* B, void* C, int M, int N,
 gsr_status run_skinny(const void* A, const void* B, void* C, int M, int N, int K, float alpha,
                     const Epi& ep,
                       cudaStream_t stream, int dev, const DeviceInfo& info) {
-    const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)));
     const int n_tiles = (N + 127) / 128;
     const int kbpt = (K + 63) / 64;
     int S = 1, P = 1;
@@ -518,8 +520,8 @@ gsr_status gemm_block(const void* A, const void* B, void* C, int64_t M, int64_t 
     if ((s = load_encoder()) != GSR_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Epi ep{gsr::kEpiScaleRelu, nullptr};
+    // (a forced small-M path, which cannot write column blocks of C, takes one-CTA tiles here)
     const int path = choose_path(M, N, K, info.num_sms);
-    if (path == 1) return GSR_ERR_INVALID_ARG;
     if (path == 2 || path == 3)
         return run_pair(path == 3 ? 128 : 256, A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info,
                         ldb, ldc);

@@ -107,7 +107,7 @@ int pair_max_active_clusters(int bn);
 int pair_smem_bytes(int bn);
 
 // Skinny path (M <= 64): C^T = B^T A^T on 128-row tiles of N, K split into slabs.
-// mp is the MMA N (16, 32 or 64).
+// mp is the MMA N (16, 32 or 64; 128 or 256 when forced for 65 to 256 rows).
 cudaError_t launch_skinny(const CUtensorMap& tmBt, const CUtensorMap& tmAt, const SkinnyParams& p,
                           int mp, cudaStream_t stream);
 

@@ -138,7 +138,9 @@ def test_path_selection_and_override():
         assert gsr.select_path(16, 8, 8) == gsr.KERNEL_TILED
         gsr.set_path_override(gsr.PATH_SKINNY)
         assert gsr.select_path(16, 8, 8) == 1
-        assert gsr.select_path(100, 8, 8) == 0      # small-M path needs M <= 64
+        assert gsr.select_path(100, 8, 8) == 1      # forced, it also takes 65 to 256 rows
+        assert gsr.select_path(256, 8, 8) == 1
+        assert gsr.select_path(257, 8, 8) == 0
     finally:
         gsr.set_path_override(gsr.PATH_AUTO)
 

@@ -39,7 +39,8 @@ def built():
                                                      (1024, 2048, 4096, gsr.PATH_PAIR_128, 0x100, 16),
                                                      (2000, 3000, 1000, gsr.PATH_PAIR, 0x100, 16),
                                                      (300, 512, 1024, gsr.PATH_TILED_64, 0x100, 1),
-                                                     (16, 4096, 8192, gsr.PATH_SKINNY, 0x200, 1)])
+                                                     (16, 4096, 8192, gsr.PATH_SKINNY, 0x200, 1),
+                                                     (200, 4096, 8192, gsr.PATH_SKINNY, 0x200, 1)])
 def test_timeout_is_reported_and_the_gpu_stays_usable(M, N, K, path, kernel, flags):
     dev = torch.device("cuda", 0)
     A, B = make_inputs(M, N, K, seed=21)

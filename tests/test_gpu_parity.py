@@ -153,6 +153,32 @@ def test_small_m_split_override(M, N, K, slabs):
     assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
 
 
+@pytest.mark.parametrize("M,N,K,rows", [(65, 264, 136, None), (100, 1000, 1000, None), (128, 520, 2048, None),
+                                         (129, 8, 8, None), (200, 4096, 512, None), (256, 640, 64, None),
+                                         (192, 16384, 1024, [0, 1, 63, 64, 127, 128, 190, 191]),
+                                         (256, 16384, 2048, [0, 1, 127, 128, 129, 200, 254, 255])])
+def test_small_m_path_forced_up_to_256_rows(M, N, K, rows):
+    # 65 to 256 rows on the small-M kernel (forced): an MMA N of 128 or 256 and the epilogue
+    # walking the accumulator in 32-column chunks, with K split into slabs (every shape but the
+    # two with N = 16384, whose 128 tiles fill the SMs alone); the split runs twice, for the
+    # same bytes (the slab order is fixed)
+    A, B = make_inputs(M, N, K, seed=M * 7 + N + K, b_std_inv_sqrt_k=True)
+    gsr.set_path_override(gsr.PATH_SKINNY)
+    try:
+        assert gsr.select_path(M, N, K) == gsr.KERNEL_SKINNY
+    finally:
+        gsr.set_path_override(gsr.PATH_AUTO)
+    C = run_gpu(A, B, 0.75, gsr.PATH_SKINNY)
+    if rows is None:
+        ref, z = oracle.gemm_scale_relu(A, B, 0.75, return_pre=True)
+        check(C, ref, z, "%dx%dx%d forced small-M" % (M, N, K))
+        C2 = run_gpu(A, B, 0.75, gsr.PATH_SKINNY)
+        assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+    else:
+        ref, z = oracle.gemm_scale_relu(A, B, 0.75, rows=rows, return_pre=True)
+        check(C[rows], ref, z, "%dx%dx%d forced small-M rows" % (M, N, K))
+
+
 @pytest.mark.parametrize("name", ["square1024", "ragged2000x3000x1000"])
 @pytest.mark.parametrize("path", [gsr.PATH_TILED_128, gsr.PATH_TILED_64, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
 def test_small_workloads_on_each_tiled_kernel(name, path):
