@@ -239,7 +239,9 @@ gsr_status gsr_release_stream(struct CUstream_st* stream);
 /* Kernel the library would run for these sizes on the current device: 0 = tiled
  * (one CTA per 128-row tile, 128 x 256, 128 x 128 or 128 x 64 tiles, whichever
  * needs fewer waves with a wave of 256-wide tiles counted as 1.45 and one of 64-wide
- * tiles as 0.9 of a wave of 128-wide ones), 1 = small-M (M <= 64),
+ * tiles as 0.9 of a wave of 128-wide ones), 1 = small-M (M <= 64, and 65 to 128
+ * rows when B holds at least 64 MiB and those one-CTA tiles would keep under two
+ * thirds of the SMs busy),
  * 2 = tiled on CTA pairs with 256 x 256 tiles (chosen when there is at least one
  * full wave of such tiles, or when K >= 6144 and 0 would use 128 x 256 tiles: the
  * pair's faster K loop then repays its larger cost per launch), 3 = tiled on CTA
@@ -252,7 +254,8 @@ int gsr_select_path(int64_t M, int64_t N, int64_t K);
 /* Forces a path for later calls (process-wide): 0 = automatic (default),
  * 1 = tiled with automatic tile width, 2 = small-M (only honoured when
  * M <= 256: 65 to 256 rows run with an MMA N of 128 or 256, which the automatic
- * choice does not take; the host-buffer entry point's blocks ignore it),
+ * choice takes only for the 65-128-row case above; the host-buffer entry point's
+ * blocks ignore it),
  * 3 = tiled with 128 x 256 tiles, 4 = tiled with 128 x 128 tiles,
  * 5 = tiled on CTA pairs with 256 x 256 tiles, 6 = tiled on CTA pairs with
  * 256 x 128 tiles, 7 = tiled with 128 x 64 tiles.

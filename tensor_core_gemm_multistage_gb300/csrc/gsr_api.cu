@@ -322,6 +322,19 @@ int tiled_width(long long mb, int64_t N, int num_sms) {
 // 1024 x 4096, 4096 x 1024, 512 x 8192); K = 16384, pairs 3.3-6.5 % (256 x 16384, 2048 x 2048).
 constexpr int64_t kPairMinK = 6144;
 
+// 65 to 128 rows: the small-M kernel with an MMA N of 128 where B is large enough for the call to
+// stream it from HBM and the one-CTA kernel's tiles would keep under two thirds of the SMs busy:
+// its K slabs then use them all.  Back to back, median of 5 x 20 calls: 65, 96 and 128 x 4096 x
+// 14336 (B 117 MB, 64 tiles of 128 x 64) 32.8-32.9 us against 43.3-43.9, 128 x 4096 x 16384 37.0
+// against 49.3, 80 x 3072 x 16384 38.9 against 56.5, 100 x 6144 x 8192 (96 tiles) 34.0 against
+// 39.3, 128 x 4096 x 8192 (B 64 MiB) 31.3 against 34.1.  Where the tiles fill more SMs it
+// loses 2-7 % (x 8192 x 8192, x 14336 x 4096) or wins little (x 16384 x 16384: 2-4 %, 128 tiles);
+// with a small B (17-34 MB, L2 flushed between calls) its split-K sums cost more than the idle
+// SMs (128 x 2048 x 4096 33.1 against 18.9, 128 x 4096 x 4096 26.7 against 21.0); and with 129 to
+// 256 rows (MMA N 256) it lost to the tiled kernels on all four large shapes.
+constexpr int kSkinnyWideMaxM = 128;
+constexpr double kSkinnyWideMinBBytes = 64.0 * (1 << 20);
+
 int choose_path(int64_t M, int64_t N, int64_t K, int num_sms) {
     const int o = g_path_override.load(std::memory_order_relaxed);
     if (o == 1 || o == 3 || o == 4 || o == 7) return 0;
@@ -332,6 +345,10 @@ int choose_path(int64_t M, int64_t N, int64_t K, int num_sms) {
     const long long pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     if (pair_tiles >= num_sms / 2) return pair_path(M, N, num_sms);
     if (K >= kPairMinK && tiled_width((M + 127) / 128, N, num_sms) == 256) return pair_path(M, N, num_sms);
+    if (M <= kSkinnyWideMaxM && 2.0 * (double)K * (double)N >= kSkinnyWideMinBBytes) {
+        const int bn = tiled_width(1, N, num_sms);
+        if (3 * ((N + bn - 1) / bn) < 2 * (int64_t)num_sms) return 1;
+    }
     return 0;
 }
 

@@ -125,6 +125,17 @@ def test_path_selection_and_override():
         assert gsr.select_path(2048, 2048, 2048) == gsr.KERNEL_TILED
         assert gsr.select_path(2048, 2048, 16384) == gsr.KERNEL_PAIR
         assert gsr.select_path(1024, 2048, 16384) == gsr.KERNEL_TILED
+        # 65 to 128 rows: the small-M kernel (MMA N 128) where B is streamed from HBM (64 MiB
+        # or more) and one-CTA tiles would keep under two thirds of the SMs busy
+        assert gsr.select_path(100, 4096, 14336) == gsr.KERNEL_SKINNY    # 64 tiles, B 117 MB
+        assert gsr.select_path(128, 4096, 16384) == gsr.KERNEL_SKINNY
+        assert gsr.select_path(96, 6144, 9216) == gsr.KERNEL_SKINNY      # 96 tiles
+        assert gsr.select_path(128, 2048, 4096) == gsr.KERNEL_TILED      # B 17 MB
+        assert gsr.select_path(128, 4096, 8192) == gsr.KERNEL_SKINNY     # B 64 MiB
+        assert gsr.select_path(128, 4096, 6144) == gsr.KERNEL_TILED      # B 48 MiB
+        assert gsr.select_path(100, 8192, 8192) == gsr.KERNEL_TILED      # 128 tiles
+        assert gsr.select_path(128, 16384, 16384) == gsr.KERNEL_TILED
+        assert gsr.select_path(129, 4096, 14336) == gsr.KERNEL_TILED
         gsr.set_path_override(gsr.PATH_TILED)
         assert gsr.select_path(16, 16384, 16384) == 0
         assert gsr.select_path(8192, 8192, 8192) == 0

@@ -179,6 +179,14 @@ def test_small_m_path_forced_up_to_256_rows(M, N, K, rows):
         check(C[rows], ref, z, "%dx%dx%d forced small-M rows" % (M, N, K))
 
 
+@pytest.mark.parametrize("M,N,K", [(100, 4096, 14336), (128, 4096, 16384), (65, 3072, 20480)])
+def test_small_m_chosen_for_up_to_128_rows(M, N, K):
+    # the automatic choice of the small-M kernel for 65-128 rows (B streamed from HBM, few
+    # one-CTA tiles)
+    assert gsr.select_path(M, N, K) == gsr.KERNEL_SKINNY
+    parity(M, N, K, 0.5, seed=M + N + K, b_scaled=True, rows=[0, 1, 31, 32, 63, 64, M - 2, M - 1])
+
+
 @pytest.mark.parametrize("name", ["square1024", "ragged2000x3000x1000"])
 @pytest.mark.parametrize("path", [gsr.PATH_TILED_128, gsr.PATH_TILED_64, gsr.PATH_PAIR, gsr.PATH_PAIR_128])
 def test_small_workloads_on_each_tiled_kernel(name, path):
