@@ -67,8 +67,10 @@ typedef enum gsr_status {
  * K == 0: C is filled with zeros (ReLU(alpha * 0)).
  *
  * Paths: M <= 64 runs the small-M kernel (B streamed once, K split across
- * SMs); larger M runs a tiled kernel, on CTA pairs with 256 x 256 tiles when
- * there are enough of them to fill the GPU, else one CTA per 128-row tile.
+ * SMs), and so do 65 to 128 rows when B is large and the tiles below would leave
+ * SMs idle; larger M runs a tiled kernel, on CTA pairs with 256 x 256 tiles when
+ * there are enough of them to fill the GPU (or K is long), else one CTA per
+ * 128-row tile (gsr_select_path gives the rules).
  *
  * Device memory the library owns: on the first call on each (device, stream)
  * pair it allocates 16 bytes for that stream (the kernels' error word and the
