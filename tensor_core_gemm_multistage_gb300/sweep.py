@@ -6,7 +6,7 @@ configuration that fits in shared memory.  Here tile shapes and pipeline depths 
 per kernel at compile time (each kernel's shared-memory budget is checked by a
 static_assert), so the runtime knobs are:
 
-  kernel   tiled 128x256, 128x128 or 128x64, CTA pair 256x256 or 256x128, small-M (M <= 64)
+  kernel   tiled 128x256, 128x128 or 128x64, CTA pair 256x256 or 256x128, small-M (M <= 256)
   raster   the grouping of tile rows for L2 reuse (gsr_set_raster_group)
   b_copy   3-D copies for B, or separate 64-column 2-D boxes (CTA-pair kernels, N % 64 == 0)
   l2       the CTA-pair kernels' L2 handling: "default" (serpentine K order across waves,
@@ -51,7 +51,7 @@ def candidates(M: int, N: int, K: int):
     """Every (kernel, raster, b_copy, l2, split) combination that is valid for this shape."""
     out = []
     for name, path in KERNELS.items():
-        if name == "small_m" and M > 64:
+        if name == "small_m" and M > 256:       # forced, the small-M kernel takes up to 256 rows
             continue
         rasters = (0,) if name == "small_m" else RASTERS
         copies = ("3d", "2d") if (name.startswith("pair_") and N % 64 == 0) else ("default",)

@@ -9,7 +9,8 @@ def test_candidates_respect_each_kernels_limits():
     big = sweep.candidates(8192, 8192, 8192)
     kernels = {c["kernel"] for c in big}
     assert kernels == {"tiled_128x256", "tiled_128x128", "tiled_128x64", "pair_256x256",
-                       "pair_256x128"}   # no small-M at M > 64
+                       "pair_256x128"}   # no small-M above 256 rows
+    assert "small_m" in {c["kernel"] for c in sweep.candidates(256, 4096, 4096)}
     assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x256"} == {"3d", "2d"}
     assert {c["b_copy"] for c in big if c["kernel"] == "pair_256x128"} == {"3d", "2d"}
     assert {c["l2"] for c in big if c["kernel"] == "pair_256x256"} == set(sweep.L2_MODES)
