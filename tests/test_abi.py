@@ -136,6 +136,10 @@ def test_path_selection_and_override():
         assert gsr.select_path(100, 8192, 8192) == gsr.KERNEL_TILED      # 128 tiles
         assert gsr.select_path(128, 16384, 16384) == gsr.KERNEL_TILED
         assert gsr.select_path(129, 4096, 14336) == gsr.KERNEL_TILED
+        # at 128 rows or fewer a 256-row pair tile is at least half empty: one-CTA tiles
+        assert gsr.select_path(100, 28672, 8192) == gsr.KERNEL_TILED
+        assert gsr.select_path(128, 65536, 4096) == gsr.KERNEL_TILED
+        assert gsr.select_path(129, 65536, 4096) == gsr.KERNEL_PAIR
         gsr.set_path_override(gsr.PATH_TILED)
         assert gsr.select_path(16, 16384, 16384) == 0
         assert gsr.select_path(8192, 8192, 8192) == 0
