@@ -244,7 +244,8 @@ gsr_status gsr_release_stream(struct CUstream_st* stream);
  * tiles as 0.9 of a wave of 128-wide ones), 1 = small-M (M <= 64, and 65 to 128
  * rows when B holds at least 64 MiB and those one-CTA tiles would keep under two
  * thirds of the SMs busy),
- * 2 = tiled on CTA pairs with 256 x 256 tiles (for more than 128 rows, chosen when
+ * 2 = tiled on CTA pairs with 256 x 256 tiles (for more than 128 rows and K above
+ * 384, where a tile is more than its epilogue, chosen when
  * there is at least one full wave of such tiles, or when K >= 6144 and 0 would use
  * 128 x 256 tiles: the pair's faster K loop then repays its larger cost per launch;
  * at 128 rows or fewer a pair tile would be at least half empty), 3 = tiled on CTA

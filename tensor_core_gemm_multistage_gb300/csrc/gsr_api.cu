@@ -321,6 +321,7 @@ int tiled_width(long long mb, int64_t N, int num_sms) {
 // 4096 x 1024, 8192 x 384); K = 8192, pairs 1.5-4.7 % faster (256 x 16384, 2048 x 2048,
 // 1024 x 4096, 4096 x 1024, 512 x 8192); K = 16384, pairs 3.3-6.5 % (256 x 16384, 2048 x 2048).
 constexpr int64_t kPairMinK = 6144;
+constexpr int64_t kPairMaxShortK = 384;
 
 // 65 to 128 rows: the small-M kernel with an MMA N of 128 where B is large enough for the call to
 // stream it from HBM and the one-CTA kernel's tiles would keep under two thirds of the SMs busy:
@@ -346,8 +347,13 @@ int choose_path(int64_t M, int64_t N, int64_t K, int num_sms) {
     // (128 rows) do the same work in one wave of half the size.  Back to back: 100 x 28672 x
     // 8192 72.0 us on 112 tiles of 128 x 256 against 91.9 on 112 pair tiles, 80 x 32768 x 4096
     // 43.0 against 56.0, 128 x 16384 x 16384 87.6 against 98.9.
+    // With a few k-blocks a tile is mostly its epilogue, and the pair's costs per tile and per
+    // launch outweigh its faster K loop: L2 flushed, 4096 x 16384 x K on 128 x 256 tiles against
+    // 256 x 256 pairs: K = 64 33.0 against 45.3 us, 256 39.2 against 47.4, 320 41.7 against 48.0,
+    // but 512 56.1 against 50.2; 8192 x 8192 x 256 39.0 against 47.4, 1496 x 18912 x 112 19.7
+    // against 25.0.  Up to K = 384 the one-CTA kernel is taken.
     const long long pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    if (M > 128) {
+    if (M > 128 && K > kPairMaxShortK) {
         if (pair_tiles >= num_sms / 2) return pair_path(M, N, num_sms);
         if (K >= kPairMinK && tiled_width((M + 127) / 128, N, num_sms) == 256) return pair_path(M, N, num_sms);
     }

@@ -138,7 +138,7 @@ CHOICE_SHAPES = [(2048, 2048, 2048), (2304, 2304, 2048), (1792, 2560, 2048), (20
                  (1024, 1024, 1024), (8192, 384, 4096), (12288, 192, 4096), (1024, 1024, 4096),
                  (1000, 1000, 200), (768, 1536, 2048), (1024, 1536, 1024), (512, 2048, 4096),
                  (1152, 2048, 1024), (256, 16384, 4096), (256, 16384, 8192), (2048, 2048, 8192),
-                 (100, 28672, 8192), (80, 32768, 4096)]
+                 (100, 28672, 8192), (80, 32768, 4096), (4096, 16384, 256), (4096, 16384, 512)]
 CHOICE_KERNELS = {"auto": gsr.PATH_AUTO, "tiled_128x256": gsr.PATH_TILED_256,
                   "tiled_128x128": gsr.PATH_TILED_128, "tiled_128x64": gsr.PATH_TILED_64,
                   "pair_256x256": gsr.PATH_PAIR,

@@ -140,6 +140,9 @@ def test_path_selection_and_override():
         assert gsr.select_path(100, 28672, 8192) == gsr.KERNEL_TILED
         assert gsr.select_path(128, 65536, 4096) == gsr.KERNEL_TILED
         assert gsr.select_path(129, 65536, 4096) == gsr.KERNEL_PAIR
+        # up to K = 384 a tile is mostly its epilogue: one-CTA tiles, not pairs
+        assert gsr.select_path(4096, 16384, 384) == gsr.KERNEL_TILED
+        assert gsr.select_path(4096, 16384, 392) == gsr.KERNEL_PAIR
         gsr.set_path_override(gsr.PATH_TILED)
         assert gsr.select_path(16, 16384, 16384) == 0
         assert gsr.select_path(8192, 8192, 8192) == 0

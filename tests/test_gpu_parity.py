@@ -368,7 +368,7 @@ def test_every_gemm_kernel_on_two_streams_at_once():
     # whatever overlaps on the GPU, each result must match the oracle
     dev = torch.device("cuda", 0)
     streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-    shapes = [(2048, 4096, 512), (1000, 1024, 512), (16, 4096, 2048), (2304, 2560, 264)]
+    shapes = [(2048, 4096, 512), (1000, 1024, 512), (16, 4096, 2048), (2304, 2560, 520)]
     cases = []
     for i, (M, N, K) in enumerate(shapes):
         A, B = make_inputs(M, N, K, seed=40 + i)
