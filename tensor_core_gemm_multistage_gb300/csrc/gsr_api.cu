@@ -263,8 +263,9 @@ int pair_full_tiles(int num_tiles, int clusters, int bn) {
 }
 
 // 0: tiled, one CTA per 128 x BN tile; 1: small-M; 2: tiled on CTA pairs (256 x 256 tiles),
-// taken when there are at least as many pair tiles as half the SMs (one full wave of pairs), or
-// below that for a long K where the one-CTA kernel would take 128 x 256 tiles (choose_path).
+// taken above 128 rows and K = 384 when there are at least as many pair tiles as half the SMs
+// (one full wave of pairs), or below that for a long K where the one-CTA kernel would take
+// 128 x 256 tiles (choose_path).
 // Pair tiles 256 wide (with a last wave of half tiles where that helps), or 128 wide where
 // that is estimated to be faster: time ~ waves x tile cost, a wave of 256 x 128 tiles or half
 // units costing kHalfTileCost of a wave of 256 x 256 tiles (half the MMAs plus the fixed
