@@ -67,8 +67,8 @@ typedef enum gsr_status {
  * K == 0: C is filled with zeros (ReLU(alpha * 0)).
  *
  * Paths: M <= 64 runs the small-M kernel (B streamed once, K split across
- * SMs), and so do 65 to 128 rows when B is large and the tiles below would leave
- * SMs idle; larger M runs a tiled kernel, on CTA pairs with 256 x 256 tiles when
+ * SMs) when B holds at least 16 MiB, and so do 65 to 128 rows when B is large and
+ * the tiles below would leave SMs idle; larger M runs a tiled kernel, on CTA pairs with 256 x 256 tiles when
  * there are enough of them to fill the GPU (or K is long), else one CTA per
  * 128-row tile (gsr_select_path gives the rules).
  *
@@ -241,7 +241,8 @@ gsr_status gsr_release_stream(struct CUstream_st* stream);
 /* Kernel the library would run for these sizes on the current device: 0 = tiled
  * (one CTA per 128-row tile, 128 x 256, 128 x 128 or 128 x 64 tiles, whichever
  * needs fewer waves with a wave of 256-wide tiles counted as 1.45 and one of 64-wide
- * tiles as 0.9 of a wave of 128-wide ones), 1 = small-M (M <= 64, and 65 to 128
+ * tiles as 0.9 of a wave of 128-wide ones), 1 = small-M (M <= 64 with B of at
+ * least 16 MiB, and 65 to 128
  * rows when B holds at least 64 MiB and those one-CTA tiles would keep under two
  * thirds of the SMs busy),
  * 2 = tiled on CTA pairs with 256 x 256 tiles (for more than 128 rows and K above

@@ -29,6 +29,13 @@ std::atomic<int> g_raster_group{0};   // 0: each kernel's default grouping
 std::atomic<int> g_split_k{0};        // 0: the small-M kernel's own slab count
 
 constexpr int kSkinnyMaxM = 64;
+// Up to 64 rows with B under 16 MiB the launch is latency-bound and one-CTA tiles finish first:
+// L2 flushed between calls, mean of 50: 64 x 1024 x 2048 13.1 us on 128 x 64 tiles against 22.5
+// on the small-M kernel, 32 x 2048 x 512 9.5 against 13.8, 64 x 5488 x 416 10.3 against 14.5,
+// 16 x 1024 x 2048 12.9 against 16.4, 16 x 4096 x 1024 12.3 against 12.6; at 32 MiB the two
+// are within ~10 % either way (16 x 4096 x 4096 18.2 on the small-M kernel against 20.5,
+// 48 x 8192 x 2048 18.3 against 16.4), and from there on B's streaming favours the small-M one.
+constexpr double kSkinnyMinBBytes = 16.0 * (1 << 20);
 // The small-M kernel also runs up to 256 rows (MMA N of 128 or 256) when forced.
 constexpr int kSkinnyMaxForcedM = 256;
 constexpr int kGroupM = 16;
@@ -343,7 +350,7 @@ int choose_path(int64_t M, int64_t N, int64_t K, int num_sms) {
     if (o == 5) return 2;
     if (o == 6) return 3;
     if (o == 2 && M <= kSkinnyMaxForcedM) return 1;
-    if (M <= kSkinnyMaxM) return 1;
+    if (M <= kSkinnyMaxM) return 2.0 * (double)K * (double)N < kSkinnyMinBBytes ? 0 : 1;
     // At 128 rows or fewer a pair tile (256 rows) is at least half empty: one-CTA tiles
     // (128 rows) do the same work in one wave of half the size.  Back to back: 100 x 28672 x
     // 8192 72.0 us on 112 tiles of 128 x 256 against 91.9 on 112 pair tiles, 80 x 32768 x 4096

@@ -98,7 +98,12 @@ def test_host_entry_validates_the_same_way():
 def test_path_selection_and_override():
     try:
         assert gsr.select_path(16, 16384, 16384) == 1
-        assert gsr.select_path(64, 8, 8) == 1
+        assert gsr.select_path(64, 8192, 8192) == 1
+        assert gsr.select_path(16, 4096, 2048) == 1          # B of exactly 16 MiB
+        # up to 64 rows with a small B the launch is latency-bound: one-CTA tiles
+        assert gsr.select_path(64, 8, 8) == gsr.KERNEL_TILED
+        assert gsr.select_path(64, 1024, 2048) == gsr.KERNEL_TILED
+        assert gsr.select_path(16, 4096, 2040) == gsr.KERNEL_TILED
         assert gsr.select_path(65, 8, 8) == gsr.KERNEL_TILED
         assert gsr.select_path(8192, 8192, 8192) == gsr.KERNEL_PAIR
         assert gsr.select_path(16384, 14336, 4096) == gsr.KERNEL_PAIR
