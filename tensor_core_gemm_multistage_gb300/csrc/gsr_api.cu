@@ -557,7 +557,8 @@ gsr_status gemm_block(const void* A, const void* B, void* C, int64_t M, int64_t 
     if ((s = load_encoder()) != GSR_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Epi ep{gsr::kEpiScaleRelu, nullptr};
-    // (a forced small-M path, which cannot write column blocks of C, takes one-CTA tiles here)
+    // (the small-M kernel cannot write column blocks of C: where it would be chosen, forced or for
+    // a block of 65-128 rows, one-CTA tiles run instead)
     const int path = choose_path(M, N, K, info.num_sms);
     if (path == 2 || path == 3)
         return run_pair(path == 3 ? 128 : 256, A, B, C, (int)M, (int)N, (int)K, alpha, ep, st, dev, info,
